@@ -1,0 +1,478 @@
+"""Benchmark of the fused AttnRes + add2 + RMSNorm epilogue on GB300.
+
+One step = one call of the whole op (fold, mixture, output norm) over one
+batch: the bandwidth workload M=8192 tokens, N=12 snapshots, H=7168, both
+addends, BF16 (about 2.0 GB moved per call; inputs larger than L2, so no L2
+flush is needed between steps).  `value` is the achieved HBM throughput in
+GB/s over all ranks (algorithmic bytes / max-over-ranks time).  The line also
+carries the decode-window latencies (M <= 32, microseconds per call), the
+roofline of the kernel, the end-to-end figure through the public API with
+host buffers, the clocks seen under load, and the CPU oracle's throughput.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU: one process per GPU (torchrun); each rank runs its own batch of
+8192 tokens (tokens are independent, no collective on the data path), so
+scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused AttnRes+add2+RMSNorm µs/call (M≤32) and HBM GB/s vs roofline (M=8192)"
+UNIT = "GB/s"
+WORKLOAD = "bandwidth-bound: M=8192 tokens, N=12 snapshots, H=7168, add2 present, BF16, N(0,1) inputs, eps=1e-6"
+M_BW, N_BW, H = 8192, 12, 7168
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attnres_fused_M8192_N12_traffic.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "kimi_k3_attention_gb300", "csrc", f)
+                  for f in ("attnres_kernel.cuh", "attnres_launch.cuh", "attnres_api.cu")]
+
+
+def algorithmic_bytes(M, N, H, has_add2=True):
+    R = M * H * 2
+    return (N + (3 if has_add2 else 2)) * R + 2 * R + 4 * H
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the kernel sources as they are now; else None."""
+    try:
+        kv = {}
+        with open(PROFILE_TRAFFIC) as f:
+            for line in f:
+                if "=" in line and not line.startswith("#"):
+                    k, v = line.split("=", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_digest") != kernel_source_digest():
+            return None
+        return int(float(kv["dram_bytes_per_launch"]))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), active=parts[4],
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8],
+                                 util=float(parts[9])))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        load = [r for r in rows if r["util"] > 0] or rows
+        reasons = set()
+        for r in load:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["smax"] for r in load),
+                "reasons": sorted(reasons), "samples": len(load)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_throughput(inp_cpu, budget_s, chunk=64, max_tokens=None):
+    """Time the CPU oracle, as it stands, on whole chunks of tokens of `inp_cpu`
+    until `budget_s` has elapsed.  Returns (GB/s, tokens, seconds, outputs)."""
+    import numpy as np
+    import torch
+    from oracle import attnres_add_rmsnorm as oracle_op
+
+    def u(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    arrs = [u(inp_cpu.prefix), u(inp_cpu.add), u(inp_cpu.add2), u(inp_cpu.bank),
+            u(inp_cpu.w), u(inp_cpu.gamma)]
+    M = inp_cpu.M
+    done, t0 = 0, time.perf_counter()
+    results = []
+    while True:
+        toks = np.arange(done, min(done + chunk, M))
+        results.append((toks, oracle_op(*arrs, inp_cpu.eps, tokens=toks, chunk=chunk)))
+        done = toks[-1] + 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= M or (max_tokens and done >= max_tokens):
+            break
+    bytes_ = algorithmic_bytes(done, inp_cpu.N, inp_cpu.H, inp_cpu.add2 is not None) - 4 * inp_cpu.H
+    return bytes_ / el / 1e9, int(done), el, results
+
+
+def cpu_info():
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except Exception:
+        pass
+    import platform
+    return model or platform.processor() or platform.machine(), os.cpu_count()
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on a bounded sample of the same
+    workload, every step a fresh chunk of 32 tokens."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    from kimi_k3_attention_gb300 import workloads as wl
+    tokens_per_step = 32
+    total = tokens_per_step * (args.steps + args.warmup)
+    inp = wl.make_inputs(total, N_BW, H, seed=4, add2=True)
+    step_times = []
+    for s in range(args.warmup + args.steps):
+        sub = wl.Inputs(inp.prefix[s * tokens_per_step:(s + 1) * tokens_per_step],
+                        inp.add[s * tokens_per_step:(s + 1) * tokens_per_step],
+                        inp.add2[s * tokens_per_step:(s + 1) * tokens_per_step],
+                        inp.bank[:, s * tokens_per_step:(s + 1) * tokens_per_step].contiguous(),
+                        inp.w, inp.gamma, inp.eps)
+        t0 = time.perf_counter()
+        oracle_throughput(sub, 0.0, chunk=tokens_per_step)
+        if s >= args.warmup:
+            step_times.append(time.perf_counter() - t0)
+    el = sum(step_times)
+    bytes_ = algorithmic_bytes(tokens_per_step, N_BW, H) * args.steps
+    value = bytes_ / el / 1e9
+    model, ncpu = cpu_info()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": f"{tokens_per_step} tokens per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{tokens_per_step} of the 8192 tokens per step, {args.steps} steps",
+                         "cpu": model, "host_cpus": ncpu},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU legs
+
+def time_bandwidth(binding, inp, steps, warmup, stream):
+    """K back-to-back calls, each bracketed by CUDA events on `stream`.
+    Returns (total seconds, per-launch seconds list)."""
+    import torch
+    out = torch.empty_like(inp.prefix)
+    newp = torch.empty_like(inp.prefix)
+    call = lambda: binding.attnres_add_rmsnorm(inp.prefix, inp.add, inp.add2, inp.bank, inp.w,  # noqa: E731
+                                               inp.gamma, inp.eps, out, newp, stream=stream, check=False)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    return call, ev, t_all0, t_all1, out, newp
+
+
+def decode_latencies(binding, wl, reps=200, graph_replays=10):
+    """Microseconds per call for the decode window (H=7168, both addends):
+    warm = CUDA-graph replay of `reps` back-to-back calls on the same buffers;
+    cold = each call timed alone by events after a 512 MB memset that evicts L2."""
+    import torch
+    res = {}
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    for M in (1, 8, 16, 32):
+        for N in (1, 3, 6, 12):
+            inp = wl.make_inputs(M, N, H, seed=900 + M * 16 + N, device="cuda")
+            out = torch.empty_like(inp.prefix)
+            newp = torch.empty_like(inp.prefix)
+
+            def call():
+                binding.attnres_add_rmsnorm(inp.prefix, inp.add, inp.add2, inp.bank, inp.w, inp.gamma,
+                                            inp.eps, out, newp, stream=s, check=False)
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    call()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(reps):
+                    call()
+            g.replay()
+            torch.cuda.synchronize()
+            warm = []
+            for _ in range(graph_replays):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                g.replay()
+                e1.record(s)
+                e1.synchronize()
+                warm.append(e0.elapsed_time(e1) * 1e3 / reps)
+            cold = []
+            with torch.cuda.stream(s):
+                for _ in range(30):
+                    flush.fill_(1)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(s)
+                    call()
+                    e1.record(s)
+                    e1.synchronize()
+                    cold.append(e0.elapsed_time(e1) * 1e3)
+            del g
+            res[f"M{M}_N{N}"] = {"warm_us": round(statistics.median(warm), 3),
+                                 "cold_us": round(statistics.median(cold), 3),
+                                 "plan": binding.attnres_plan(M, N, H)}
+    del flush
+    torch.cuda.synchronize()
+    return res
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    from kimi_k3_attention_gb300 import binding
+    from kimi_k3_attention_gb300 import workloads as wl
+    from kimi_k3_attention_gb300.build import LIB, build
+    if not os.path.exists(LIB):
+        build()
+    binding.load()
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if ws == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- the bandwidth workload, resident in HBM
+    inp = wl.bandwidth_inputs(device="cuda", seed=4 + rank)
+    stream = torch.cuda.Stream()
+    call, ev, t0, t1, out, newp = time_bandwidth(binding, inp, args.steps, args.warmup, stream)
+    nbytes = algorithmic_bytes(M_BW, N_BW, H)
+
+    # soak: ~1.5 s of the same calls so that the clock samples see steady load
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ts = time.perf_counter()
+        while time.perf_counter() - ts < 1.5:
+            for _ in range(20):
+                call()
+            stream.synchronize()
+    barrier()
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            a.record(stream)
+            call()
+            b.record(stream)
+    t1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    total_s = t0.elapsed_time(t1) / 1e3
+    launch_s = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    total_s = max_over_ranks(total_s)
+    avg_launch = max_over_ranks(sum(launch_s) / len(launch_s))
+    value = nbytes * ws * args.steps / total_s / 1e9
+
+    # ---- end to end through the public API with pinned host buffers
+    host = {k: getattr(inp, k).cpu().pin_memory() for k in ("prefix", "add", "add2", "bank", "w", "gamma")}
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    newp_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dev = {k: torch.empty_like(getattr(inp, k)) for k in host}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = 2 * out.numel() * out.element_size()
+
+    def e2e_step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        binding.attnres_add_rmsnorm(dev["prefix"], dev["add"], dev["add2"], dev["bank"], dev["w"],
+                                    dev["gamma"], inp.eps, out, newp, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        newp_h.copy_(newp, non_blocking=True)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3)
+    e2e_value = nbytes * ws * args.steps / e2e_s / 1e9
+    del dev, host, out_h, newp_h
+
+    decode = None
+    cpu_base = None
+    if rank == 0 and not args.no_decode:
+        decode = decode_latencies(binding, wl)
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle on the first tokens of this same workload; the GPU's
+        # outputs for those tokens are checked against it on the way
+        import numpy as np
+        from oracle import check_out
+        os.environ.setdefault("OMP_NUM_THREADS", "1")
+        n_sample = 1024
+        cpu_inp = wl.Inputs(inp.prefix[:n_sample].cpu(), inp.add[:n_sample].cpu(),
+                            inp.add2[:n_sample].cpu(), inp.bank[:, :n_sample].cpu().contiguous(),
+                            inp.w.cpu(), inp.gamma.cpu(), inp.eps)
+        gbs, done, el, results = oracle_throughput(cpu_inp, args.cpu_seconds)
+
+        def u(t):
+            return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+        g_np, g_out = u(newp[:done]), u(out[:done])
+        parity = True
+        for toks, (rnp, rout, rb) in results:
+            parity &= bool((g_np[toks] == rnp).all()) and check_out(g_out[toks], rout, rb)["ok"]
+        model, ncpu = cpu_info()
+        cpu_base = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                    "sample": f"first {done} of the 8192 tokens, {el:.1f} s",
+                    "cpu": model, "host_cpus": ncpu, "gpu_outputs_match_on_sample": parity}
+
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = peaks()
+    achieved = nbytes / avg_launch / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_s / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, f32 arithmetic",
+        "data": "synthetic (seeded N(0,1) BF16 tensors)",
+        "config": {"workload": WORKLOAD, "M": M_BW, "N": N_BW, "H": H, "add2": True,
+                   "bytes_per_call": nbytes, "l2": "inputs (2.0 GB) larger than L2, no flush",
+                   "plan": binding.attnres_plan(M_BW, N_BW, H),
+                   "parallelism": f"dp{ws} (each rank its own 8192 tokens)"},
+        "us_per_call": round(total_s / args.steps * 1e6, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
+                     "traffic": profiled_traffic(), "algorithmic_bytes": nbytes,
+                     "avg_launch_us": round(avg_launch * 1e6, 2)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s / args.steps * 1e3, 3)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "decode_us_per_call": decode,
+        "cpu_baseline": cpu_base,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-decode", action="store_true", help="skip the M<=32 latency table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

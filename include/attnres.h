@@ -1,0 +1,151 @@
+/*
+ * attnres.h -- C ABI of the GB300 (sm_103a) fused AttnRes + add2 + RMSNorm
+ * decode-layer epilogue.
+ *
+ * The operation, per token m of M (H columns, all tensors BF16):
+ *
+ *   1. Fold of the deferred MoE tail into the prefix sum.
+ *        s          = bf16(add + add2)     (s = add when add2 is NULL)
+ *        new_prefix = bf16(prefix + s)
+ *      Both additions are float32 round-to-nearest-even with subnormals kept
+ *      (no flush to zero); each result is rounded to BF16 to nearest even.
+ *      This is bit for bit the result of the two BF16 tensor additions.
+ *      Defined in: TensorRT-LLM PR #20546 ("Kimi K3: fold the MoE-tail
+ *      additions into the next attention-residual"), section "Op", the
+ *      optional trailing layer_residual_add2 of attn_res_add_rmsnorm_fwd.
+ *   2. Attention-residual depth mixture over the N bank snapshots
+ *      v_0..v_{N-1} = bank[0..N-1, m, :] and the updated prefix
+ *      v_N = new_prefix[m, :]:
+ *        l_i   = w . RMSNorm(v_i) = (w . v_i) / sqrt(mean(v_i^2) + eps)
+ *        alpha = softmax(l)
+ *        h     = sum_i alpha_i v_i                   (float32)
+ *   3. out = bf16( h / sqrt(mean(h^2) + eps) * gamma ), one final rounding.
+ *      Steps 2-3 are the attention-residual + RMSNorm consumer that the same
+ *      PR page names (sections "Description" and "Op"); the page does not
+ *      write their math out, and the form above is the specification this
+ *      library implements.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are BF16 stored as 16-bit words, row-major, contiguous, in
+ *     device memory of the current CUDA device, each 16-byte aligned.
+ *     [M,H] tensors have row stride H; the bank is [N,M,H] (snapshot-major:
+ *     snapshot i of token m starts at element (i*M + m)*H).
+ *   - The caller owns every buffer.  The library allocates nothing per call,
+ *     keeps no pointer after the call returns, and needs no workspace.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
+ *     nothing is synchronised on the host.
+ *   - Arguments are validated on the host before any launch; a rejected call
+ *     launches nothing and returns a negative status.  A failed launch returns
+ *     ATTNRES_ERR_CUDA and attnres_last_cuda_error() holds the cudaError_t.
+ *     No entry point aborts, traps or prints.
+ *   - Aliasing: new_prefix may be exactly prefix (in-place carry-on of the
+ *     prefix sum) or any region that overlaps no input (e.g. bank slot N,
+ *     which the call does not read).  out may overlap nothing.
+ *   - Results are deterministic: the same inputs give the same bits on every
+ *     call, whatever the launch configuration of the same variant and cluster
+ *     size; new_prefix is bit-identical across all configurations.
+ */
+#ifndef ATTNRES_H
+#define ATTNRES_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st* attnres_stream_t;
+
+typedef enum {
+  ATTNRES_OK = 0,
+  ATTNRES_ERR_NULL = -1,    /* a required pointer is NULL                  */
+  ATTNRES_ERR_SHAPE = -2,   /* M < 1, N not in [1,12], H not a multiple of 8
+                               or H outside [8, 16384]                     */
+  ATTNRES_ERR_ALIGN = -3,   /* a pointer is not 16-byte aligned            */
+  ATTNRES_ERR_ALIAS = -4,   /* out overlaps a tensor, or new_prefix overlaps
+                               an input other than exactly prefix          */
+  ATTNRES_ERR_EPS = -5,     /* eps is not finite and > 0                   */
+  ATTNRES_ERR_CUDA = -6,    /* a CUDA runtime call failed                  */
+  ATTNRES_ERR_DEVICE = -7,  /* the current device is not compute 10.3      */
+  ATTNRES_ERR_CONFIG = -8   /* a forced launch configuration is invalid    */
+} attnres_status;
+
+#define ATTNRES_MAX_N 12
+#define ATTNRES_MAX_H 16384
+
+/*
+ * attnres_add_rmsnorm -- the fused epilogue (steps 1-3 above).
+ *
+ *   prefix      [M,H]   prefix sum before this layer (layer_residual)
+ *   add         [M,H]   first deferred addend (routed MoE output)
+ *   add2        [M,H]   second addend (shared-expert output) or NULL: with
+ *                       NULL the fold is new_prefix = bf16(prefix + add)
+ *   bank        [N,M,H] depth bank of snapshots, 1 <= N <= 12
+ *   w           [H]     per-layer pseudo-query of the mixture
+ *   gamma       [H]     RMSNorm weight of the output norm
+ *   eps                 epsilon of both RMSNorms, finite and > 0
+ *   out         [M,H]   output: RMSNorm(h) * gamma
+ *   new_prefix  [M,H]   output: the updated prefix sum
+ *   M, N, H             tokens, snapshots, hidden size (H = 7168 in the model)
+ *   stream              CUDA stream of the launch
+ *
+ * N = 0 ("no snapshots yet") and N > 12 are rejected with ATTNRES_ERR_SHAPE:
+ * the PR's fallbacks for those cases add first and run another path.
+ * The launch configuration is chosen from (M, N, H) and the SM count.
+ */
+int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
+                        const void* bank, const void* w, const void* gamma,
+                        float eps, void* out, void* new_prefix,
+                        int M, int N, int H, attnres_stream_t stream);
+
+/*
+ * Launch configuration, for tests and benchmarks that pin one.
+ *   variant   0 = automatic (same as attnres_add_rmsnorm);
+ *             1 = one CTA per token, 16 columns per thread;
+ *             2 = a thread-block cluster of `cluster` CTAs per token, each
+ *                 CTA owning a contiguous 1/cluster of the columns, 8 columns
+ *                 per thread; the per-token sums are exchanged through
+ *                 distributed shared memory.
+ *   cluster   CTAs per token for variant 2 (1..16); 0 = automatic.
+ *   threads   threads per CTA (multiple of 32, up to 1024; for variant 2 at
+ *             most 256 and cluster * threads/32 <= 32); 0 = the smallest
+ *             count that covers the CTA's columns.
+ *   grid_tokens  CTAs (clusters) along the token axis, each looping over
+ *             tokens with this stride; 0 = min(M, 65535).
+ */
+typedef struct {
+  int variant;
+  int cluster;
+  int threads;
+  int grid_tokens;
+} attnres_config;
+
+/* The fused epilogue with a pinned configuration (cfg may be NULL = auto).
+ * An unusable cfg returns ATTNRES_ERR_CONFIG without launching. */
+int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const void* add2,
+                           const void* bank, const void* w, const void* gamma,
+                           float eps, void* out, void* new_prefix,
+                           int M, int N, int H, attnres_stream_t stream,
+                           const attnres_config* cfg);
+
+/* The configuration attnres_add_rmsnorm would launch for (M, N, H) on the
+ * current device, written to *plan (all four fields resolved).  Returns a
+ * status; needs a CUDA device (it reads the SM count). */
+int attnres_plan(int M, int N, int H, attnres_config* plan);
+
+/* Static description of a status code; never NULL. */
+const char* attnres_status_string(int status);
+
+/* cudaError_t of the last failing CUDA call made by this thread inside the
+ * library (0 if none). */
+int attnres_last_cuda_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int attnres_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNRES_H */

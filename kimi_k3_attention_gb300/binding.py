@@ -1,0 +1,170 @@
+"""Thin ctypes binding of libattnres.so (include/attnres.h).
+
+Argument marshalling only: every step of the op runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors used as device buffers; their data
+pointers and the current torch stream are handed to the C ABI.  If the shared
+library is missing the first call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libattnres.so")
+
+STATUS = {
+    0: "ATTNRES_OK", -1: "ATTNRES_ERR_NULL", -2: "ATTNRES_ERR_SHAPE", -3: "ATTNRES_ERR_ALIGN",
+    -4: "ATTNRES_ERR_ALIAS", -5: "ATTNRES_ERR_EPS", -6: "ATTNRES_ERR_CUDA",
+    -7: "ATTNRES_ERR_DEVICE", -8: "ATTNRES_ERR_CONFIG",
+}
+VARIANTS = {"auto": 0, "cta": 1, "cluster": 2}
+
+# Every symbol include/attnres.h declares.
+EXPORTS = (
+    "attnres_add_rmsnorm",
+    "attnres_add_rmsnorm_ex",
+    "attnres_plan",
+    "attnres_status_string",
+    "attnres_last_cuda_error",
+    "attnres_version",
+)
+
+
+class AttnResError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("cluster", ctypes.c_int),
+                ("threads", ctypes.c_int), ("grid_tokens", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the shared library once; raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} not found: build it with kimi_k3_attention_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    args = [vp, vp, vp, vp, vp, vp, f, vp, vp, i, i, i, vp]
+    lib.attnres_add_rmsnorm.argtypes = args
+    lib.attnres_add_rmsnorm.restype = i
+    lib.attnres_add_rmsnorm_ex.argtypes = args + [ctypes.POINTER(Config)]
+    lib.attnres_add_rmsnorm_ex.restype = i
+    lib.attnres_plan.argtypes = [i, i, i, ctypes.POINTER(Config)]
+    lib.attnres_plan.restype = i
+    lib.attnres_status_string.argtypes = [i]
+    lib.attnres_status_string.restype = ctypes.c_char_p
+    lib.attnres_last_cuda_error.argtypes = []
+    lib.attnres_last_cuda_error.restype = i
+    lib.attnres_version.argtypes = []
+    lib.attnres_version.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().attnres_status_string(int(status)).decode()
+
+
+def _check(status: int):
+    if status != 0:
+        lib = load()
+        msg = lib.attnres_status_string(status).decode()
+        if status == -6:
+            msg += f" (cudaError {lib.attnres_last_cuda_error()})"
+        raise AttnResError(status, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_config(variant="auto", cluster=0, threads=0, grid_tokens=0) -> Config:
+    v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    return Config(v, int(cluster), int(threads), int(grid_tokens))
+
+
+def _check_tensor(name, t, shape=None):
+    import torch
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, out, new_prefix,
+                        stream=None, config: Optional[Config] = None, check=True):
+    """Launch the fused epilogue on torch CUDA tensors (see include/attnres.h).
+
+    prefix, add, add2 (or None), out, new_prefix: [M, H]; bank: [N, M, H];
+    w, gamma: [H]; all bfloat16, contiguous, on the current device.
+    stream: a torch.cuda.Stream (default: the current stream).
+    config: a Config pinning the launch (default: the library's choice).
+    """
+    N, M, H = bank.shape
+    if check:
+        for name, t, shp in (("prefix", prefix, (M, H)), ("add", add, (M, H)),
+                             ("bank", bank, (N, M, H)), ("w", w, (H,)), ("gamma", gamma, (H,)),
+                             ("out", out, (M, H)), ("new_prefix", new_prefix, (M, H))):
+            _check_tensor(name, t, shp)
+        if add2 is not None:
+            _check_tensor("add2", add2, (M, H))
+    lib = load()
+    s = _stream_handle(stream)
+    if config is None:
+        st = lib.attnres_add_rmsnorm(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(bank), _ptr(w),
+                                     _ptr(gamma), float(eps), _ptr(out), _ptr(new_prefix),
+                                     M, N, H, s)
+    else:
+        st = lib.attnres_add_rmsnorm_ex(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(bank), _ptr(w),
+                                        _ptr(gamma), float(eps), _ptr(out), _ptr(new_prefix),
+                                        M, N, H, s, ctypes.byref(config))
+    _check(st)
+
+
+def attnres_add_rmsnorm_raw(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, M, N, H,
+                            stream=0, config: Optional[Config] = None) -> int:
+    """The C entry point on raw integer pointers; returns the status code."""
+    lib = load()
+    vp = ctypes.c_void_p
+    args = [vp(prefix), vp(add), vp(add2) if add2 else None, vp(bank), vp(w), vp(gamma),
+            float(eps), vp(out), vp(new_prefix), int(M), int(N), int(H), vp(stream)]
+    if config is None:
+        return lib.attnres_add_rmsnorm(*args)
+    return lib.attnres_add_rmsnorm_ex(*args, ctypes.byref(config))
+
+
+def attnres_plan(M, N, H) -> dict:
+    c = Config()
+    _check(load().attnres_plan(int(M), int(N), int(H), ctypes.byref(c)))
+    return c.as_dict()
+
+
+def version() -> int:
+    return load().attnres_version()

@@ -1,0 +1,230 @@
+// C ABI of the fused AttnRes + add2 + RMSNorm epilogue: argument validation,
+// choice of launch configuration, dispatch to the compiled instantiations.
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "../../include/attnres.h"
+#include "attnres_launch.cuh"
+
+namespace attnres {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+struct DeviceInfo {
+  std::atomic<int> state{0};  // 0 unknown, 1 ok, 2 wrong architecture
+  std::atomic<int> sms{0};
+};
+DeviceInfo g_dev[kMaxDevices];
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return ATTNRES_ERR_CUDA;
+}
+
+// Compute capability 10.3 (GB300) and SM count of the current device.
+int current_device(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTNRES_ERR_DEVICE;
+  DeviceInfo& d = g_dev[dev];
+  int st = d.state.load(std::memory_order_acquire);
+  if (st == 0) {
+    int major = 0, minor = 0, count = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return fail_cuda(e);
+    d.sms.store(count, std::memory_order_relaxed);
+    st = (major == 10 && minor == 3) ? 1 : 2;
+    d.state.store(st, std::memory_order_release);
+  }
+  if (st != 1) return ATTNRES_ERR_DEVICE;
+  *sms = d.sms.load(std::memory_order_relaxed);
+  return ATTNRES_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+int validate(const void* prefix, const void* add, const void* add2, const void* bank,
+             const void* w, const void* gamma, float eps, const void* out,
+             const void* new_prefix, int M, int N, int H) {
+  if (!prefix || !add || !bank || !w || !gamma || !out || !new_prefix) return ATTNRES_ERR_NULL;
+  if (M < 1 || N < 1 || N > ATTNRES_MAX_N || H < 8 || H > ATTNRES_MAX_H || (H % 8) != 0)
+    return ATTNRES_ERR_SHAPE;
+  if (!(eps > 0.f) || !isfinite(eps)) return ATTNRES_ERR_EPS;
+  if (misaligned(prefix) || misaligned(add) || (add2 && misaligned(add2)) || misaligned(bank) ||
+      misaligned(w) || misaligned(gamma) || misaligned(out) || misaligned(new_prefix))
+    return ATTNRES_ERR_ALIGN;
+  const size_t R = static_cast<size_t>(M) * static_cast<size_t>(H) * 2u;
+  const size_t B = R * static_cast<size_t>(N);
+  const size_t V = static_cast<size_t>(H) * 2u;
+  const void* ins[6] = {prefix, add, add2, bank, w, gamma};
+  const size_t insz[6] = {R, R, add2 ? R : 0, B, V, V};
+  for (int i = 0; i < 6; ++i)
+    if (overlaps(out, R, ins[i], insz[i])) return ATTNRES_ERR_ALIAS;
+  if (overlaps(out, R, new_prefix, R)) return ATTNRES_ERR_ALIAS;
+  for (int i = 0; i < 6; ++i) {
+    if (i == 0 && new_prefix == prefix) continue;  // in-place carry-on
+    if (overlaps(new_prefix, R, ins[i], insz[i])) return ATTNRES_ERR_ALIAS;
+  }
+  return ATTNRES_OK;
+}
+
+int round_up32(int x) { return (x + 31) & ~31; }
+
+// Fill every zero field of *c for (M, H) on a device with `sms` SMs, then
+// check the result.  Returns ATTNRES_OK or ATTNRES_ERR_CONFIG.
+int resolve(int M, int H, int sms, attnres_config* c) {
+  const int H8 = H / 8;
+  if (c->variant == 0) {
+    c->variant = 2;
+    if (c->cluster == 0) {
+      // Latency regime: spread each token over enough CTAs that M * cluster
+      // covers the SMs; streaming regime: the smallest cluster whose CTAs
+      // fit the split shape, so several tokens are in flight per SM.
+      int cl = 1;
+      while (round_up32((H8 + cl - 1) / cl) > kSplitMaxT) ++cl;
+      if (M <= 64) {
+        while (cl < 16 && M * cl < sms) cl *= 2;
+        if (cl > 16) cl = 16;
+      } else if (cl < 4 && round_up32((H8 + 3) / 4) <= kSplitMaxT && H8 >= 4 * 64) {
+        cl = 4;
+      }
+      c->cluster = cl;
+    }
+  }
+  if (c->variant == 1) {
+    if (c->cluster == 0) c->cluster = 1;
+    if (c->cluster != 1) return ATTNRES_ERR_CONFIG;
+    const int need = round_up32((H8 + kCtaVPT - 1) / kCtaVPT);
+    if (c->threads == 0) c->threads = need;
+    if (c->threads < need || c->threads > kCtaMaxT || (c->threads % 32) != 0)
+      return ATTNRES_ERR_CONFIG;
+  } else if (c->variant == 2) {
+    if (c->cluster == 0) {
+      int cl = 1;
+      while (round_up32((H8 + cl - 1) / cl) > kSplitMaxT) ++cl;
+      c->cluster = cl;
+    }
+    if (c->cluster < 1 || c->cluster > 16) return ATTNRES_ERR_CONFIG;
+    const int cpc = (H8 + c->cluster - 1) / c->cluster;
+    const int need = round_up32((cpc + kSplitVPT - 1) / kSplitVPT);
+    if (c->threads == 0) c->threads = need;
+    if (c->threads < need || c->threads > kSplitMaxT || (c->threads % 32) != 0)
+      return ATTNRES_ERR_CONFIG;
+  } else {
+    return ATTNRES_ERR_CONFIG;
+  }
+  if (c->grid_tokens == 0) c->grid_tokens = M < 65535 ? M : 65535;
+  if (c->grid_tokens < 1 || c->grid_tokens > 65535) return ATTNRES_ERR_CONFIG;
+  return ATTNRES_OK;
+}
+
+template <int VPT, int MAXT>
+cudaError_t dispatch(int N, bool add2, const Params& p, dim3 g, int t, int c, cudaStream_t s) {
+#define ATTNRES_CASE(n)                                                          \
+  case n:                                                                        \
+    return add2 ? launch_fused<n, true, VPT, MAXT>(p, g, t, c, s)                \
+                : launch_fused<n, false, VPT, MAXT>(p, g, t, c, s);
+  switch (N) {
+    ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
+    ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
+    ATTNRES_CASE(9) ATTNRES_CASE(10) ATTNRES_CASE(11) ATTNRES_CASE(12)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef ATTNRES_CASE
+}
+
+}  // namespace
+}  // namespace attnres
+
+using namespace attnres;
+
+extern "C" int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const void* add2,
+                                      const void* bank, const void* w, const void* gamma,
+                                      float eps, void* out, void* new_prefix, int M, int N,
+                                      int H, attnres_stream_t stream,
+                                      const attnres_config* cfg) {
+  int st = validate(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, M, N, H);
+  if (st != ATTNRES_OK) return st;
+  int sms = 0;
+  if ((st = current_device(&sms)) != ATTNRES_OK) return st;
+  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0};
+  if ((st = resolve(M, H, sms, &c)) != ATTNRES_OK) return st;
+
+  Params p;
+  p.prefix = static_cast<const uint4*>(prefix);
+  p.add = static_cast<const uint4*>(add);
+  p.add2 = static_cast<const uint4*>(add2);
+  p.bank = static_cast<const uint4*>(bank);
+  p.w = static_cast<const uint4*>(w);
+  p.gamma = static_cast<const uint4*>(gamma);
+  p.out = static_cast<uint4*>(out);
+  p.new_prefix = static_cast<uint4*>(new_prefix);
+  p.M = M;
+  p.H8 = H / 8;
+  p.bank_stride = static_cast<long long>(M) * p.H8;
+  p.cpc = (p.H8 + c.cluster - 1) / c.cluster;
+  p.eps = eps;
+  p.inv_h = 1.0f / static_cast<float>(H);
+
+  const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool has_add2 = add2 != nullptr;
+  cudaError_t e = (c.variant == 1)
+                      ? dispatch<kCtaVPT, kCtaMaxT>(N, has_add2, p, grid, c.threads, 1, s)
+                      : dispatch<kSplitVPT, kSplitMaxT>(N, has_add2, p, grid, c.threads, c.cluster, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ATTNRES_OK;
+}
+
+extern "C" int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
+                                   const void* bank, const void* w, const void* gamma, float eps,
+                                   void* out, void* new_prefix, int M, int N, int H,
+                                   attnres_stream_t stream) {
+  return attnres_add_rmsnorm_ex(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, M, N, H,
+                                stream, nullptr);
+}
+
+extern "C" int attnres_plan(int M, int N, int H, attnres_config* plan) {
+  if (!plan) return ATTNRES_ERR_NULL;
+  if (M < 1 || N < 1 || N > ATTNRES_MAX_N || H < 8 || H > ATTNRES_MAX_H || (H % 8) != 0)
+    return ATTNRES_ERR_SHAPE;
+  int sms = 0;
+  int st = current_device(&sms);
+  if (st != ATTNRES_OK) return st;
+  attnres_config c = {0, 0, 0, 0};
+  if ((st = resolve(M, H, sms, &c)) != ATTNRES_OK) return st;
+  *plan = c;
+  return ATTNRES_OK;
+}
+
+extern "C" const char* attnres_status_string(int status) {
+  switch (status) {
+    case ATTNRES_OK: return "ok";
+    case ATTNRES_ERR_NULL: return "a required pointer is NULL";
+    case ATTNRES_ERR_SHAPE: return "unsupported shape: need M >= 1, 1 <= N <= 12, 8 <= H <= 16384, H % 8 == 0";
+    case ATTNRES_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case ATTNRES_ERR_ALIAS: return "out overlaps a tensor, or new_prefix overlaps an input other than prefix";
+    case ATTNRES_ERR_EPS: return "eps must be finite and > 0";
+    case ATTNRES_ERR_CUDA: return "a CUDA runtime call failed (see attnres_last_cuda_error)";
+    case ATTNRES_ERR_DEVICE: return "the current device is not a compute capability 10.3 GPU";
+    case ATTNRES_ERR_CONFIG: return "invalid launch configuration";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int attnres_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" int attnres_version(void) { return 100; }

@@ -1,0 +1,371 @@
+// Device code of the fused AttnRes + add2 + RMSNorm epilogue (sm_103a).
+//
+// One token is processed by a thread-block cluster of C CTAs (C = 1 is a
+// single CTA).  CTA c of the cluster owns a contiguous slice of the token's
+// H/8 sixteen-byte chunks; every thread owns VPT chunks of every source row
+// and keeps them in registers from the single HBM read to the final store:
+//
+//   load    prefix, add, add2, bank[0..N-1] chunks (16-byte vector loads)
+//   fold    new_prefix = bf16(prefix + bf16(add + add2)) with add.rn.f32 and
+//           cvt.rn.bf16x2.f32 written in PTX, so no fast-math flag can turn
+//           them into flush-to-zero forms (TensorRT-LLM PR #20546, "Op")
+//   stats   ss_i = sum v^2 and d_i = w.v for the N+1 sources, one pass
+//   R1      2(N+1) partial sums: warp transpose-reduction, CTA sum in shared
+//           memory, cluster exchange through distributed shared memory
+//   softmax every warp evaluates logits and softmax redundantly from the same
+//           totals in the same order, so all warps of all CTAs agree bitwise
+//   mix     h = sum_i alpha_i v_i from registers (no second read)
+//   R2      sum h^2: warp reduction, cluster exchange
+//   out     bf16(h * rsqrt(mean(h^2) + eps) * gamma)
+//
+// Every reduction has a fixed order, so results are deterministic.  The
+// kernel has no spin-waits: the only waits are the hardware CTA and cluster
+// barriers, which every thread of every CTA reaches on the same path.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attnres {
+
+struct Params {
+  const uint4* prefix;
+  const uint4* add;
+  const uint4* add2;
+  const uint4* bank;
+  const uint4* w;
+  const uint4* gamma;
+  uint4* out;
+  uint4* new_prefix;
+  long long bank_stride;  // chunks between snapshots: M * H8
+  int M;
+  int H8;                 // 16-byte chunks per row: H / 8
+  int cpc;                // chunks owned by one CTA of the cluster
+  float eps;
+  float inv_h;            // 1 / H
+};
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_keep(const uint4* p) {
+  uint4 r;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_out(uint4* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// float32 addition, round to nearest even, subnormals kept (no .ftz).
+__device__ __forceinline__ float add_rn(float a, float b) {
+  float r;
+  asm("add.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// Two float32 -> packed BF16x2, each rounded to nearest even (no .ftz form
+// exists for this conversion; subnormal results are kept).  `lo` lands in
+// the low 16 bits.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// BF16 halves of a 32-bit word -> exact float32 (integer moves only).
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ float elem(const uint4& v, int e) {
+  const uint32_t u = (e < 2) ? v.x : (e < 4) ? v.y : (e < 6) ? v.z : v.w;
+  return (e & 1) ? bf_hi(u) : bf_lo(u);
+}
+
+// One 32-bit word (two BF16 lanes) of the fold.
+template <bool ADD2>
+__device__ __forceinline__ uint32_t fold_word(uint32_t p, uint32_t a, uint32_t a2) {
+  uint32_t s = a;
+  if (ADD2) s = pack_bf16x2(add_rn(bf_lo(a), bf_lo(a2)), add_rn(bf_hi(a), bf_hi(a2)));
+  return pack_bf16x2(add_rn(bf_lo(p), bf_lo(s)), add_rn(bf_hi(p), bf_hi(s)));
+}
+
+template <bool ADD2>
+__device__ __forceinline__ uint4 fold_chunk(const uint4& p, const uint4& a, const uint4& a2) {
+  uint4 r;
+  r.x = fold_word<ADD2>(p.x, a.x, a2.x);
+  r.y = fold_word<ADD2>(p.y, a.y, a2.y);
+  r.z = fold_word<ADD2>(p.z, a.z, a2.z);
+  r.w = fold_word<ADD2>(p.w, a.w, a2.w);
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// XOR-butterfly sums: every lane ends with the same bits, because each step
+// adds the same two operands (in either order) in every lane of a pair.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+
+// Transpose-reduction of KP (a power of two <= 32) values per lane across the
+// warp with KP-1 + (5 - log2 KP) shuffles.  Afterwards lane l holds the warp
+// total of value index l >> (5 - log2 KP); lanes sharing an index agree.
+template <int KP>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[KP], int lane) {
+#pragma unroll
+  for (int half = KP / 2, o = 16; half >= 1; half >>= 1, o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float give = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(FULL, give, o);
+    }
+  }
+  float r = v[0];
+  constexpr int LOGKP = (KP >= 32) ? 5 : (KP >= 16) ? 4 : (KP >= 8) ? 3 : (KP >= 4) ? 2 : 1;
+  // lanes that differ only in the low 5 - log2(KP) bits hold partial sums of
+  // the same index: finish them with plain butterfly steps
+  constexpr int FIRST = (LOGKP < 5) ? (1 << (4 - LOGKP)) : 0;
+#pragma unroll
+  for (int o = FIRST; o > 0; o >>= 1) r += __shfl_xor_sync(FULL, r, o);
+  return r;
+}
+
+template <int K>
+struct Pow2 {
+  static constexpr int value = K <= 2 ? 2 : K <= 4 ? 4 : K <= 8 ? 8 : K <= 16 ? 16 : 32;
+  static constexpr int log2 = K <= 2 ? 1 : K <= 4 ? 2 : K <= 8 ? 3 : K <= 16 ? 4 : 5;
+};
+
+// ---------------------------------------------------------------- the kernel
+
+template <int N, bool ADD2, int VPT, int MAXT>
+__global__ void __launch_bounds__(MAXT) attnres_fused_kernel(const Params p) {
+  constexpr int S = N + 1;             // sources: bank[0..N-1], new prefix
+  constexpr int K = 2 * S;             // per-token sums: (ss_i, d_i)
+  constexpr int KP = Pow2<K>::value;
+  constexpr int SHIFT = 5 - Pow2<K>::log2;
+
+  __shared__ float red[32][KP];        // per-warp partials of R1
+  __shared__ float xchg[KP];           // CTA totals of R1, read by the cluster
+  __shared__ float red2[32];           // per-warp sum of h^2, read by the cluster
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t csize = cluster_nctarank();
+  const int c0 = static_cast<int>(crank) * p.cpc;
+  const int cend = min(c0 + p.cpc, p.H8);
+
+  int jj[VPT];
+  bool ok[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    jj[k] = c0 + tid + k * static_cast<int>(blockDim.x);
+    ok[k] = jj[k] < cend;
+  }
+
+  uint4 wv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) wv[k] = ok[k] ? ld_keep(p.w + jj[k]) : make_uint4(0, 0, 0, 0);
+
+  for (int m = blockIdx.y; m < p.M; m += gridDim.y) {
+    const size_t row = static_cast<size_t>(m) * p.H8;
+
+    // ---- load every source chunk once
+    uint4 v[S][VPT];
+    uint4 pr[VPT], ad[VPT], ad2[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      pr[k] = ok[k] ? ld_stream(p.prefix + row + jj[k]) : z;
+      ad[k] = ok[k] ? ld_stream(p.add + row + jj[k]) : z;
+      ad2[k] = (ADD2 && ok[k]) ? ld_stream(p.add2 + row + jj[k]) : z;
+#pragma unroll
+      for (int i = 0; i < N; ++i)
+        v[i][k] = ok[k] ? ld_stream(p.bank + i * p.bank_stride + row + jj[k]) : z;
+    }
+
+    // ---- fold, store the updated prefix
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      v[N][k] = fold_chunk<ADD2>(pr[k], ad[k], ad2[k]);
+      if (ok[k]) st_out(p.new_prefix + row + jj[k], v[N][k]);
+    }
+
+    // ---- per-source sums of squares and dot products with w
+    float part[KP];
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+      float ss = 0.f, d = 0.f;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x = elem(v[i][k], e);
+          ss = __fmaf_rn(x, x, ss);
+          d = __fmaf_rn(elem(wv[k], e), x, d);
+        }
+      }
+      part[2 * i] = ss;
+      part[2 * i + 1] = d;
+    }
+#pragma unroll
+    for (int i = K; i < KP; ++i) part[i] = 0.f;
+    // Keep only the packed BF16 words alive across the reductions: without
+    // this the compiler reuses the unpacked floats of the pass above in the
+    // mixture and holds twice the registers.
+#pragma unroll
+    for (int i = 0; i < S; ++i)
+#pragma unroll
+      for (int k = 0; k < VPT; ++k)
+        asm volatile("" : "+r"(v[i][k].x), "+r"(v[i][k].y), "+r"(v[i][k].z), "+r"(v[i][k].w));
+
+    // ---- R1: warp, CTA, cluster
+    const float wtot = warp_transpose_reduce<KP>(part, lane);
+    if ((lane & ((1 << SHIFT) - 1)) == 0) red[warp][lane >> SHIFT] = wtot;
+    __syncthreads();
+    if (warp == 0 && lane < KP) {
+      float s = 0.f;
+      for (int w = 0; w < nwarps; ++w) s += red[w][lane];
+      xchg[lane] = s;
+    }
+    cluster_sync();
+    float tot = 0.f;
+    if (lane < KP) {
+      for (uint32_t c = 0; c < csize; ++c) tot += ld_dsmem(dsmem_addr(&xchg[lane], c));
+    }
+
+    // ---- logits and softmax, lane i < S holds source i
+    const float ss_i = __shfl_sync(FULL, tot, (2 * lane) & 31);
+    const float d_i = __shfl_sync(FULL, tot, (2 * lane + 1) & 31);
+    const float logit = (lane < S) ? rsqrtf(__fmaf_rn(ss_i, p.inv_h, p.eps)) * d_i : -INFINITY;
+    const float mx = warp_max(logit);
+    const float ex = (lane < S) ? __expf(logit - mx) : 0.f;
+    const float den = warp_sum(ex);
+    const float alpha_l = ex / den;
+    float alpha[S];
+#pragma unroll
+    for (int i = 0; i < S; ++i) alpha[i] = __shfl_sync(FULL, alpha_l, i);
+
+    uint4 gv[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) gv[k] = ok[k] ? ld_keep(p.gamma + jj[k]) : make_uint4(0, 0, 0, 0);
+
+    // ---- mixture h = sum_i alpha_i v_i, and sum h^2
+    float h[VPT][8];
+    float q = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float acc = __fmul_rn(alpha[0], elem(v[0][k], e));
+#pragma unroll
+        for (int i = 1; i < S; ++i) acc = __fmaf_rn(alpha[i], elem(v[i][k], e), acc);
+        h[k][e] = acc;
+        q = __fmaf_rn(acc, acc, q);
+      }
+    }
+
+    // ---- R2: warp, then every warp reads all warps of all CTAs
+    q = warp_sum(q);
+    if (lane == 0) red2[warp] = q;
+    cluster_sync();
+    const int nw_total = static_cast<int>(csize) * nwarps;
+    float qq = 0.f;
+    for (int idx = lane; idx < nw_total; idx += 32)
+      qq += ld_dsmem(dsmem_addr(&red2[idx % nwarps], static_cast<uint32_t>(idx / nwarps)));
+    qq = warp_sum(qq);
+    cluster_arrive();  // this CTA is done reading the cluster's shared memory
+    const float rh = rsqrtf(__fmaf_rn(qq, p.inv_h, p.eps));
+
+    // ---- output
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      if (ok[k]) {
+        uint4 o;
+        o.x = pack_bf16x2(__fmul_rn(__fmul_rn(h[k][0], rh), elem(gv[k], 0)),
+                          __fmul_rn(__fmul_rn(h[k][1], rh), elem(gv[k], 1)));
+        o.y = pack_bf16x2(__fmul_rn(__fmul_rn(h[k][2], rh), elem(gv[k], 2)),
+                          __fmul_rn(__fmul_rn(h[k][3], rh), elem(gv[k], 3)));
+        o.z = pack_bf16x2(__fmul_rn(__fmul_rn(h[k][4], rh), elem(gv[k], 4)),
+                          __fmul_rn(__fmul_rn(h[k][5], rh), elem(gv[k], 5)));
+        o.w = pack_bf16x2(__fmul_rn(__fmul_rn(h[k][6], rh), elem(gv[k], 6)),
+                          __fmul_rn(__fmul_rn(h[k][7], rh), elem(gv[k], 7)));
+        st_out(p.out + row + jj[k], o);
+      }
+    }
+    // No CTA may leave, or overwrite its exchange slots for the next token,
+    // while another CTA of the cluster may still read them.
+    cluster_wait();
+  }
+}
+
+// Host-side launcher of one instantiation (defined in attnres_launch.cuh).
+template <int N, bool ADD2, int VPT, int MAXT>
+cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, cudaStream_t s);
+
+}  // namespace attnres

@@ -1,0 +1,56 @@
+// Host-side launch of one instantiation of the fused kernel, and the
+// explicit-instantiation macro used by the attnres_inst_*.cu units.
+#pragma once
+
+#include <atomic>
+
+#include "attnres_kernel.cuh"
+
+namespace attnres {
+
+constexpr int kMaxDevices = 64;
+
+// The two compiled shapes of the kernel.
+//   split: 8 columns per thread, up to 256 threads (cluster of CTAs per token)
+//   cta:   16 columns per thread, up to 448 threads (one CTA per token)
+constexpr int kSplitVPT = 1, kSplitMaxT = 256;
+constexpr int kCtaVPT = 2, kCtaMaxT = 448;
+
+template <int N, bool ADD2, int VPT, int MAXT>
+cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, cudaStream_t s) {
+  auto kern = attnres_fused_kernel<N, ADD2, VPT, MAXT>;
+  // Cluster sizes above 8 need an opt-in per function and device.
+  static std::atomic<unsigned char> opted[kMaxDevices];
+  if (cluster > 8) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!opted[dev].load(std::memory_order_acquire)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      opted[dev].store(1, std::memory_order_release);
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+#define ATTNRES_INSTANTIATE(N, ADD2)                                                        \
+  template cudaError_t launch_fused<N, ADD2, kSplitVPT, kSplitMaxT>(const Params&, dim3, int, \
+                                                                     int, cudaStream_t);      \
+  template cudaError_t launch_fused<N, ADD2, kCtaVPT, kCtaMaxT>(const Params&, dim3, int, int, \
+                                                                 cudaStream_t);
+
+}  // namespace attnres

@@ -1,0 +1,97 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, and rejects bad arguments on the host before any CUDA call.
+(Pointers here are fake addresses; validation never dereferences them.)"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from kimi_k3_attention_gb300 import binding
+from kimi_k3_attention_gb300.build import LIB
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attnres.h")
+
+pytestmark = pytest.mark.skipif(not os.path.exists(LIB), reason="libattnres.so not built")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attnres_\w+)\s*\(", src)))
+
+
+def test_header_declarations_are_exported():
+    lib = ctypes.CDLL(LIB)
+    names = _declared()
+    assert set(names) == set(binding.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version():
+    for code in binding.STATUS:
+        assert binding.status_string(code)
+    assert binding.status_string(12345) == "unknown status"
+    assert binding.version() >= 100
+
+
+M, N, H = 4, 3, 64
+R = M * H * 2
+BASE = 1 << 32
+
+
+def _layout():
+    """Disjoint fake device regions, 16-byte aligned."""
+    off = [0]
+
+    def take(n):
+        a = BASE + off[0]
+        off[0] += (n + 4095) // 4096 * 4096
+        return a
+    return dict(prefix=take(R), add=take(R), add2=take(R), bank=take(N * R), w=take(2 * H),
+                gamma=take(2 * H), out=take(R), new_prefix=take(R))
+
+
+def _call(**kw):
+    a = _layout()
+    a.update({k: v for k, v in kw.items() if k in a})
+    shape = dict(M=M, N=N, H=H, eps=1e-6)
+    shape.update({k: v for k, v in kw.items() if k in shape})
+    return binding.attnres_add_rmsnorm_raw(a["prefix"], a["add"], a["add2"], a["bank"], a["w"],
+                                           a["gamma"], shape["eps"], a["out"], a["new_prefix"],
+                                           shape["M"], shape["N"], shape["H"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(prefix=0), -1), (dict(add=0), -1), (dict(bank=0), -1), (dict(w=0), -1),
+    (dict(gamma=0), -1), (dict(out=0), -1), (dict(new_prefix=0), -1),
+    (dict(N=0), -2), (dict(N=13), -2), (dict(M=0), -2), (dict(H=12), -2), (dict(H=0), -2),
+    (dict(H=16392), -2),
+    (dict(eps=0.0), -5), (dict(eps=-1e-6), -5), (dict(eps=float("inf")), -5), (dict(eps=float("nan")), -5),
+    (dict(prefix=BASE + 8), -3), (dict(bank=BASE + (1 << 20) + 2), -3), (dict(out=BASE + (9 << 20) + 4), -3),
+])
+def test_invalid_arguments_rejected(kw, code):
+    assert _call(**kw) == code
+
+
+def test_alias_rules():
+    a = _layout()
+    # out inside the bank
+    assert _call(out=a["bank"] + 16) == -4
+    # out equal to new_prefix
+    assert _call(out=a["new_prefix"]) == -4
+    # out overlapping w
+    assert _call(out=a["w"] - 16) == -4
+    # new_prefix overlapping add2, or partly overlapping prefix
+    assert _call(new_prefix=a["add2"] + 32) == -4
+    assert _call(new_prefix=a["prefix"] + 16) == -4
+    # new_prefix inside the bank snapshots the call reads
+    assert _call(new_prefix=a["bank"] + R) == -4
+
+
+def test_config_struct_layout():
+    c = binding.make_config("cluster", cluster=8, threads=128)
+    assert ctypes.sizeof(c) == 16
+    assert c.as_dict() == {"variant": 2, "cluster": 8, "threads": 128, "grid_tokens": 0}

@@ -1,0 +1,318 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on the
+seeded workloads: new_prefix bit-exact, out within the tolerance of
+oracle/tolerance.py (2 BF16 ulp with a 2^-16 floor; |delta| <= 1.5e-2 where
+|out| <= 4)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from kimi_k3_attention_gb300 import binding
+from kimi_k3_attention_gb300 import workloads as wl
+from oracle import bf16_decode, fold
+
+from gpu_helpers import Guarded, assert_parity, cfg_name, run_gpu, split_configs, u16
+
+pytestmark = pytest.mark.gpu
+
+H = wl.H_MODEL
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load()
+
+
+# ---------------------------------------------------------------- PR reference case
+
+@pytest.mark.parametrize("cfg", split_configs(H), ids=cfg_name)
+def test_pr_reference_case_every_variant(cfg):
+    inp = wl.pr_reference_case()
+    gnp, gout = run_gpu(inp, cfg)
+    assert_parity(inp, gnp, gout, label=cfg_name(cfg))
+
+
+# ---------------------------------------------------------------- decode sweep
+
+@pytest.mark.parametrize("case", list(wl.decode_sweep_cases()), ids=lambda c: f"M{c[1]}-N{c[2]}-{'add2' if c[3] else 'noadd2'}")
+def test_decode_sweep_auto(case):
+    idx, M, N, has_add2 = case
+    inp = wl.decode_sweep_inputs(idx, M, N, has_add2)
+    gnp, gout = run_gpu(inp)
+    assert_parity(inp, gnp, gout, label=f"case {idx}")
+
+
+@pytest.mark.parametrize("cfg", split_configs(H)[1:], ids=cfg_name)
+@pytest.mark.parametrize("M,N", [(1, 12), (32, 12), (16, 5), (8, 1)])
+def test_decode_every_variant(cfg, M, N):
+    inp = wl.make_inputs(M, N, H, seed=77 + M + N, add2=True)
+    gnp, gout = run_gpu(inp, cfg)
+    assert_parity(inp, gnp, gout, label=cfg_name(cfg))
+
+
+# ---------------------------------------------------------------- bit-exactness stress
+
+@pytest.mark.parametrize("special_prefix", [False, True])
+@pytest.mark.parametrize("cfg", [None, binding.make_config("cluster", cluster=4),
+                                 binding.make_config("cta")], ids=cfg_name)
+def test_bit_exact_stress(special_prefix, cfg):
+    inp = wl.stress_inputs(special_prefix=special_prefix)
+    gnp, gout = run_gpu(inp, cfg)
+    assert_parity(inp, gnp, gout)
+    if special_prefix:
+        # subnormal sums must reach the updated prefix (exponent field 0, non-zero)
+        sub = ((gnp & 0x7F80) == 0) & ((gnp & 0x7F) != 0)
+        assert sub.sum() > 1000
+
+
+def test_golden_fold_cases_on_gpu(golden_dir):
+    rows = []
+    for line in open(os.path.join(golden_dir, "fold_cases.txt")):
+        if line.strip() and not line.startswith("#"):
+            rows.append([int(x, 16) for x in line.split()[:4]])
+    rows = np.array(rows, dtype=np.uint16)
+    n = len(rows)
+    Hs = 8 * ((n + 7) // 8)
+    p = np.zeros(Hs, np.uint16)
+    a = np.zeros(Hs, np.uint16)
+    a2 = np.zeros(Hs, np.uint16)
+    e = np.zeros(Hs, np.uint16)
+    p[:n], a[:n], a2[:n], e[:n] = rows.T
+    t = lambda x: torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16)  # noqa: E731
+    inp = wl.make_inputs(1, 1, Hs, seed=3)
+    inp.prefix, inp.add, inp.add2 = t(p)[None], t(a)[None], t(a2)[None]
+    for cfg in (None, binding.make_config("cta"), binding.make_config("cluster", cluster=1)):
+        gnp, _ = run_gpu(inp, cfg)
+        assert (gnp[0, :n] == e[:n]).all(), [hex(x) for x in gnp[0, :n]]
+
+
+def test_fold_sweep_all_patterns():
+    """Every finite BF16 add against 64 add2 patterns (all exponents, both
+    signs, subnormals), with prefix zero and random: bit-exact to the oracle."""
+    allb = np.arange(65536, dtype=np.uint16)
+    allb = allb[np.isfinite(bf16_decode(allb))]
+    rng = np.random.default_rng(9)
+    picks = np.concatenate([np.arange(0, 0x7F80, 0x7F80 // 24, dtype=np.uint16)[:24],
+                            rng.integers(1, 128, 8).astype(np.uint16)])
+    picks = np.concatenate([picks, picks | 0x8000])
+    Hs = 8192
+    M = -(-allb.size * picks.size // Hs)
+    total = M * Hs
+    a = np.resize(allb, total).astype(np.uint16)
+    a2 = np.repeat(picks, -(-total // picks.size))[:total].astype(np.uint16)
+    for prefix_kind in ("zero", "random"):
+        if prefix_kind == "zero":
+            p = np.zeros(total, np.uint16)
+        else:
+            p = rng.integers(0, 65536, total).astype(np.uint16)
+            p = np.where(np.isfinite(bf16_decode(p)), p, 0).astype(np.uint16)
+        ref, _ = fold(p, a, a2)
+        ok = np.isfinite(bf16_decode(ref))
+        t = lambda x: torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).view(M, Hs)  # noqa: E731
+        inp = wl.make_inputs(M, 1, Hs, seed=5)
+        inp.prefix, inp.add, inp.add2 = t(p), t(a), t(a2)
+        inp.bank.zero_()
+        gnp, _ = run_gpu(inp)
+        bad = np.flatnonzero((gnp.ravel() != ref) & ok)
+        assert bad.size == 0, (prefix_kind, hex(p[bad[0]]), hex(a[bad[0]]), hex(a2[bad[0]]),
+                               hex(gnp.ravel()[bad[0]]), hex(ref[bad[0]]))
+
+
+# ---------------------------------------------------------------- 25-layer chain
+
+def _chain_gpu(fused, M=8):
+    emb, p0, layers = wl.chain_inputs(M=M)
+    dev = "cuda"
+    bank = [emb.to(dev)]
+    P = p0.to(dev)
+    taps, prefixes = [], []
+    for li, L in enumerate(layers):
+        w, g = L.w.to(dev), L.gamma.to(dev)
+        r, s = L.routed.to(dev), L.shared.to(dev)
+        if fused:
+            a, a2 = r, s
+        else:
+            a, a2 = r + s, None          # PyTorch's BF16 addition first
+        b = torch.stack(bank).contiguous()
+        out = torch.empty_like(P)
+        newp = torch.empty_like(P)
+        binding.attnres_add_rmsnorm(P, a, a2, b, w, g, wl.EPS, out, newp)
+        P = newp
+        taps.append(u16(out))
+        prefixes.append(u16(newp))
+        if wl.chain_appends_after(li):
+            bank.append(P.clone())
+    torch.cuda.synchronize()
+    return u16(torch.stack(bank)), prefixes, taps
+
+
+def test_chain_fused_equals_eager_bitwise_and_oracle():
+    bf, pf, tf = _chain_gpu(True)
+    be, pe, te = _chain_gpu(False)
+    assert bf.shape[0] == 12
+    assert (bf == be).all()
+    for a, b in zip(pf, pe):
+        assert (a == b).all()
+    for a, b in zip(tf, te):
+        assert (a == b).all()
+    # and layer by layer against the oracle on the same inputs
+    from oracle import attnres_add_rmsnorm as oop, check_out
+    emb, p0, layers = wl.chain_inputs(M=8)
+    bank = [u16(emb)]
+    P = u16(p0)
+    for li, L in enumerate(layers):
+        npb, out, bound = oop(P, u16(L.routed), u16(L.shared), np.stack(bank), u16(L.w),
+                              u16(L.gamma), wl.EPS)
+        assert (npb == pf[li]).all(), li
+        r = check_out(tf[li], out, bound)
+        assert r["ok"], (li, r)
+        P = npb
+        if wl.chain_appends_after(li):
+            bank.append(P.copy())
+
+
+# ---------------------------------------------------------------- invariants on the GPU
+
+@pytest.mark.parametrize("cfg", [None, binding.make_config("cta"),
+                                 binding.make_config("cluster", cluster=16)], ids=cfg_name)
+def test_two_addends_equal_one_presummed_addend(cfg):
+    """Section "Test Coverage": two addends give bitwise the same updated
+    prefix sum and output as one addend holding their BF16 sum."""
+    for M, N in ((1, 1), (8, 7), (16, 12), (32, 3)):
+        inp = wl.make_inputs(M, N, H, seed=500 + M * 13 + N, add2=True)
+        gnp2, gout2 = run_gpu(inp, cfg)
+        pre = wl.Inputs(inp.prefix, inp.add + inp.add2, None, inp.bank, inp.w, inp.gamma, inp.eps)
+        gnp1, gout1 = run_gpu(pre, cfg)
+        assert (gnp1 == gnp2).all() and (gout1 == gout2).all()
+        # and the same prefix as PyTorch's prefix + (routed + shared)
+        assert (u16(inp.prefix + (inp.add + inp.add2)) == gnp2).all()
+
+
+def test_deterministic_repeats():
+    inp = wl.make_inputs(32, 12, H, seed=42).to("cuda")
+    outs = []
+    for _ in range(5):
+        out = torch.empty_like(inp.prefix)
+        newp = torch.empty_like(inp.prefix)
+        binding.attnres_add_rmsnorm(inp.prefix, inp.add, inp.add2, inp.bank, inp.w, inp.gamma,
+                                    inp.eps, out, newp)
+        outs.append((u16(out), u16(newp)))
+    for o in outs[1:]:
+        assert (o[0] == outs[0][0]).all() and (o[1] == outs[0][1]).all()
+
+
+def test_all_split_cluster_sizes_agree_on_new_prefix():
+    inp = wl.make_inputs(16, 9, H, seed=43)
+    ref = None
+    for cfg in split_configs(H):
+        gnp, _ = run_gpu(inp, cfg)
+        if ref is None:
+            ref = gnp
+        assert (gnp == ref).all(), cfg_name(cfg)
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("Hs", [8, 16, 24, 64, 72, 1000, 2056, 7176, 8192, 16384])
+def test_ragged_and_small_hidden_sizes(Hs):
+    for M, N, add2 in ((1, 1, True), (3, 12, False), (5, 4, True)):
+        inp = wl.make_inputs(M, N, Hs, seed=Hs + M + N, add2=add2)
+        for cfg in split_configs(Hs):
+            gnp, gout = run_gpu(inp, cfg)
+            assert_parity(inp, gnp, gout, label=f"H={Hs} {cfg_name(cfg)}")
+
+
+@pytest.mark.parametrize("grid_tokens", [1, 3, 64])
+def test_token_loop(grid_tokens):
+    """Fewer token CTAs than tokens: each cluster loops over tokens."""
+    inp = wl.make_inputs(67, 6, H, seed=11)
+    for cl in (4, 8):
+        cfg = binding.make_config("cluster", cluster=cl, grid_tokens=grid_tokens)
+        gnp, gout = run_gpu(inp, cfg)
+        assert_parity(inp, gnp, gout)
+    gnp, gout = run_gpu(inp, binding.make_config("cta", grid_tokens=grid_tokens))
+    assert_parity(inp, gnp, gout)
+
+
+def test_more_tokens_than_grid_limit():
+    """M above 65535: the grid's token axis is capped and clusters loop."""
+    M, Hs = 70000, 64
+    inp = wl.make_inputs(M, 2, Hs, seed=12, device="cuda")
+    gnp, gout = run_gpu(inp)
+    toks = np.array([0, 1, 65534, 65535, 65536, 69999])
+    assert_parity(inp, gnp, gout, tokens=toks)
+
+
+def test_in_place_prefix_and_bank_slot_target():
+    inp = wl.make_inputs(8, 5, H, seed=21)
+    ref_np, ref_out = run_gpu(inp)
+    d = inp.to("cuda")
+    # in place: new_prefix is prefix
+    P = d.prefix.clone()
+    out = torch.empty_like(P)
+    binding.attnres_add_rmsnorm(P, d.add, d.add2, d.bank, d.w, d.gamma, d.eps, out, P)
+    torch.cuda.synchronize()
+    assert (u16(P) == ref_np).all() and (u16(out) == ref_out).all()
+    # new_prefix written straight into bank slot N of a bank with N+1 slots
+    big = torch.empty((6, 8, H), dtype=torch.bfloat16, device="cuda")
+    big[:5] = d.bank
+    out2 = torch.empty_like(P)
+    binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, big[:5], d.w, d.gamma, d.eps, out2, big[5])
+    torch.cuda.synchronize()
+    assert (u16(big[5]) == ref_np).all() and (u16(out2) == ref_out).all()
+
+
+def test_side_stream_and_plan():
+    inp = wl.make_inputs(16, 12, H, seed=31)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        gnp, gout = run_gpu(inp, stream=s)
+    assert_parity(inp, gnp, gout)
+    for M in (1, 8, 16, 32, 8192):
+        plan = binding.attnres_plan(M, 12, H)
+        assert plan["variant"] in (1, 2) and plan["threads"] % 32 == 0
+
+
+def test_invalid_config_rejected_on_device():
+    d = wl.make_inputs(4, 3, H, seed=1).to("cuda")
+    out = torch.empty_like(d.prefix)
+    newp = torch.empty_like(d.prefix)
+    for cfg in (binding.make_config("cluster", cluster=17), binding.make_config("cluster", cluster=1),
+                binding.make_config("cta", cluster=2), binding.make_config(7),
+                binding.make_config("cluster", cluster=8, threads=100)):
+        with pytest.raises(binding.AttnResError) as e:
+            binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps,
+                                        out, newp, config=cfg)
+        assert e.value.status == -8
+
+
+def test_subnormal_inputs_in_the_mixture():
+    """All sources tiny (BF16 subnormal scale): outputs stay finite and within
+    tolerance (the norms divide by sqrt(mean + eps))."""
+    inp = wl.make_inputs(4, 3, H, seed=8)
+    for name in ("prefix", "add", "add2"):
+        setattr(inp, name, (getattr(inp, name).float() * 1e-39).to(torch.bfloat16))
+    inp.bank = (inp.bank.float() * 1e-39).to(torch.bfloat16)
+    gnp, gout = run_gpu(inp)
+    assert_parity(inp, gnp, gout)
+
+
+# ---------------------------------------------------------------- full size, sampled
+
+def test_bandwidth_config_sampled():
+    """M=8192, N=12, H=7168, add2 present, in the automatic launch
+    configuration the benchmark times: new_prefix checked for every token
+    against the oracle's fold, out for 48 sampled tokens."""
+    inp = wl.bandwidth_inputs(device="cuda")
+    gnp, gout = run_gpu(inp)
+    P, A, A2 = u16(inp.prefix), u16(inp.add), u16(inp.add2)
+    for t0 in range(0, inp.M, 1024):
+        ref, _ = fold(P[t0:t0 + 1024], A[t0:t0 + 1024], A2[t0:t0 + 1024])
+        assert (gnp[t0:t0 + 1024] == ref).all(), t0
+    rng = np.random.default_rng(0)
+    toks = np.unique(np.concatenate([[0, 1, 151, 152, 4095, 8190, 8191], rng.integers(0, 8192, 41)]))
+    cpu = inp.to("cpu")
+    assert_parity(cpu, gnp, gout, tokens=toks)
