@@ -304,66 +304,11 @@ def decode_latencies(binding, wl, reps=200, graph_replays=10):
     return res
 
 
-def run_ours(args):
+def run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_over_ranks, ws):
+    """The same metric through the public API with pinned host buffers: every
+    step copies the inputs host->device, calls the op, and copies both
+    outputs back, all on the launching stream inside the timed region."""
     import torch
-    import torch.distributed as dist
-
-    ws, rank, local = dist_env()
-    if ws > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    from kimi_k3_attention_gb300 import binding
-    from kimi_k3_attention_gb300 import workloads as wl
-    from kimi_k3_attention_gb300.build import LIB, build
-    if not os.path.exists(LIB):
-        build()
-    binding.load()
-
-    def barrier():
-        if ws > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    def max_over_ranks(x):
-        if ws == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    # ---- the bandwidth workload, resident in HBM
-    inp = wl.bandwidth_inputs(device="cuda", seed=4 + rank)
-    stream = torch.cuda.Stream()
-    call, ev, t0, t1, out, newp = time_bandwidth(binding, inp, args.steps, args.warmup, stream)
-    nbytes = algorithmic_bytes(M_BW, N_BW, H)
-
-    # soak: ~1.5 s of the same calls so that the clock samples see steady load
-    sampler = ClockSampler(torch.cuda.current_device())
-    sampler.start()
-    time.sleep(0.3)
-    with torch.cuda.stream(stream):
-        ts = time.perf_counter()
-        while time.perf_counter() - ts < 1.5:
-            for _ in range(20):
-                call()
-            stream.synchronize()
-    barrier()
-    t0.record(stream)
-    with torch.cuda.stream(stream):
-        for a, b in ev:
-            a.record(stream)
-            call()
-            b.record(stream)
-    t1.record(stream)
-    barrier()
-    clocks = sampler.stop()
-    total_s = t0.elapsed_time(t1) / 1e3
-    launch_s = [a.elapsed_time(b) / 1e3 for a, b in ev]
-    total_s = max_over_ranks(total_s)
-    avg_launch = max_over_ranks(sum(launch_s) / len(launch_s))
-    value = nbytes * ws * args.steps / total_s / 1e9
-
-    # ---- end to end through the public API with pinned host buffers
     host = {k: getattr(inp, k).cpu().pin_memory() for k in ("prefix", "add", "add2", "bank", "w", "gamma")}
     out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     newp_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
@@ -392,6 +337,75 @@ def run_ours(args):
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3)
     e2e_value = nbytes * ws * args.steps / e2e_s / 1e9
     del dev, host, out_h, newp_h
+    return {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s / args.steps * 1e3, 3)}
+
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    from kimi_k3_attention_gb300 import binding
+    from kimi_k3_attention_gb300 import workloads as wl
+    from kimi_k3_attention_gb300.build import LIB, build
+    if not os.path.exists(LIB):
+        build()
+    binding.load()
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if ws == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- the bandwidth workload, resident in HBM
+    M = args.tokens
+    inp = wl.bandwidth_inputs(device="cuda", seed=4 + rank, M=M)
+    stream = torch.cuda.Stream()
+    call, ev, t0, t1, out, newp = time_bandwidth(binding, inp, args.steps, args.warmup, stream)
+    nbytes = algorithmic_bytes(M, N_BW, H)
+
+    # soak: the same calls back to back so that the clock samples see steady load
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ts = time.perf_counter()
+        while time.perf_counter() - ts < args.soak_seconds:
+            for _ in range(20):
+                call()
+            stream.synchronize()
+    barrier()
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            a.record(stream)
+            call()
+            b.record(stream)
+    t1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    total_s = t0.elapsed_time(t1) / 1e3
+    launch_s = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    total_s = max_over_ranks(total_s)
+    avg_launch = max_over_ranks(sum(launch_s) / len(launch_s))
+    value = nbytes * ws * args.steps / total_s / 1e9
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_over_ranks, ws)
 
     decode = None
     cpu_base = None
@@ -434,17 +448,16 @@ def run_ours(args):
         "ms_per_step": round(total_s / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, f32 arithmetic",
         "data": "synthetic (seeded N(0,1) BF16 tensors)",
-        "config": {"workload": WORKLOAD, "M": M_BW, "N": N_BW, "H": H, "add2": True,
+        "config": {"workload": WORKLOAD if M == M_BW else WORKLOAD.replace("M=8192", f"M={M}"), "M": M, "N": N_BW, "H": H, "add2": True,
                    "bytes_per_call": nbytes, "l2": "inputs (2.0 GB) larger than L2, no flush",
-                   "plan": binding.attnres_plan(M_BW, N_BW, H),
+                   "plan": binding.attnres_plan(M, N_BW, H),
                    "parallelism": f"dp{ws} (each rank its own 8192 tokens)"},
         "us_per_call": round(total_s / args.steps * 1e6, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
                      "traffic": profiled_traffic(), "algorithmic_bytes": nbytes,
                      "avg_launch_us": round(avg_launch * 1e6, 2)},
-        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s / args.steps * 1e3, 3)},
+        "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
         "decode_us_per_call": decode,
@@ -466,6 +479,11 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true", help="skip the M<=32 latency table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--soak-seconds", type=float, default=1.5,
+                    help="back-to-back calls before the timed region, under the clock sampler")
+    ap.add_argument("--tokens", type=int, default=M_BW,
+                    help="tokens of the bandwidth workload (smaller only for profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

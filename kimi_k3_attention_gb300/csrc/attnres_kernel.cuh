@@ -78,6 +78,22 @@ __device__ __forceinline__ float add_rn(float a, float b) {
   return r;
 }
 
+// float32 fused multiply-add and multiply, round to nearest even, subnormal
+// inputs and results kept.  Written in PTX so that a fast-math build (which
+// turns the compiler's own float32 arithmetic into .ftz forms) cannot flush
+// the mixture of tiny sources to zero.
+__device__ __forceinline__ float fma_rn(float a, float b, float c) {
+  float r;
+  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ float mul_rn(float a, float b) {
+  float r;
+  asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 // Two float32 -> packed BF16x2, each rounded to nearest even (no .ftz form
 // exists for this conversion; subnormal results are kept).  `lo` lands in
 // the low 16 bits.
@@ -266,8 +282,8 @@ __global__ void __launch_bounds__(MAXT) attnres_fused_kernel(const Params p) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float x = elem(v[i][k], e);
-          ss = __fmaf_rn(x, x, ss);
-          d = __fmaf_rn(elem(wv[k], e), x, d);
+          ss = fma_rn(x, x, ss);
+          d = fma_rn(elem(wv[k], e), x, d);
         }
       }
       part[2 * i] = ss;
@@ -322,11 +338,11 @@ __global__ void __launch_bounds__(MAXT) attnres_fused_kernel(const Params p) {
     for (int k = 0; k < VPT; ++k) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        float acc = __fmul_rn(alpha[0], elem(v[0][k], e));
+        float acc = mul_rn(alpha[0], elem(v[0][k], e));
 #pragma unroll
-        for (int i = 1; i < S; ++i) acc = __fmaf_rn(alpha[i], elem(v[i][k], e), acc);
+        for (int i = 1; i < S; ++i) acc = fma_rn(alpha[i], elem(v[i][k], e), acc);
         h[k][e] = acc;
-        q = __fmaf_rn(acc, acc, q);
+        q = fma_rn(acc, acc, q);
       }
     }
 
@@ -347,14 +363,14 @@ __global__ void __launch_bounds__(MAXT) attnres_fused_kernel(const Params p) {
     for (int k = 0; k < VPT; ++k) {
       if (ok[k]) {
         uint4 o;
-        o.x = pack_bf16x2(__fmul_rn(__fmul_rn(h[k][0], rh), elem(gv[k], 0)),
-                          __fmul_rn(__fmul_rn(h[k][1], rh), elem(gv[k], 1)));
-        o.y = pack_bf16x2(__fmul_rn(__fmul_rn(h[k][2], rh), elem(gv[k], 2)),
-                          __fmul_rn(__fmul_rn(h[k][3], rh), elem(gv[k], 3)));
-        o.z = pack_bf16x2(__fmul_rn(__fmul_rn(h[k][4], rh), elem(gv[k], 4)),
-                          __fmul_rn(__fmul_rn(h[k][5], rh), elem(gv[k], 5)));
-        o.w = pack_bf16x2(__fmul_rn(__fmul_rn(h[k][6], rh), elem(gv[k], 6)),
-                          __fmul_rn(__fmul_rn(h[k][7], rh), elem(gv[k], 7)));
+        o.x = pack_bf16x2(mul_rn(mul_rn(h[k][0], rh), elem(gv[k], 0)),
+                          mul_rn(mul_rn(h[k][1], rh), elem(gv[k], 1)));
+        o.y = pack_bf16x2(mul_rn(mul_rn(h[k][2], rh), elem(gv[k], 2)),
+                          mul_rn(mul_rn(h[k][3], rh), elem(gv[k], 3)));
+        o.z = pack_bf16x2(mul_rn(mul_rn(h[k][4], rh), elem(gv[k], 4)),
+                          mul_rn(mul_rn(h[k][5], rh), elem(gv[k], 5)));
+        o.w = pack_bf16x2(mul_rn(mul_rn(h[k][6], rh), elem(gv[k], 6)),
+                          mul_rn(mul_rn(h[k][7], rh), elem(gv[k], 7)));
         st_out(p.out + row + jj[k], o);
       }
     }
