@@ -51,6 +51,29 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_seed(rank):
+    """Every rank draws its own 8192-token batch (weak scaling)."""
+    return 4 + rank
+
+
+def max_over_ranks(x, device):
+    """Max of a host float over all ranks of the default process group (the
+    timing rule: the slowest rank sets the time); identity when not
+    distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(nbytes_per_call, world_size, steps, seconds):
+    """Whole-job GB/s: every rank moved nbytes_per_call per step."""
+    return nbytes_per_call * world_size * steps / seconds / 1e9
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -250,61 +273,74 @@ def time_bandwidth(binding, inp, steps, warmup, stream):
     return call, ev, t_all0, t_all1, out, newp
 
 
-def decode_latencies(binding, wl, reps=200, graph_replays=10):
-    """Microseconds per call for the decode window (H=7168, both addends):
-    warm = CUDA-graph replay of `reps` back-to-back calls on the same buffers;
-    cold = each call timed alone by events after a 512 MB memset that evicts L2."""
+def decode_latencies(binding, wl, reps=200, replays=5):
+    """Microseconds per call in the decode window (H=7168, both addends), from
+    CUDA-graph replays of back-to-back calls on one stream:
+      warm: `reps` calls on the same buffers (inputs L2-resident);
+      cold: calls cycling through distinct buffer sets whose total exceeds
+            2.5x the L2 size, so every call reads its inputs from HBM.
+    Each figure is the median over `replays` replays of graph time / calls."""
     import torch
-    res = {}
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or (128 << 20)
     s = torch.cuda.Stream()
+    res = {}
     for M in (1, 8, 16, 32):
         for N in (1, 3, 6, 12):
-            inp = wl.make_inputs(M, N, H, seed=900 + M * 16 + N, device="cuda")
-            out = torch.empty_like(inp.prefix)
-            newp = torch.empty_like(inp.prefix)
+            per_set = algorithmic_bytes(M, N, H)
+            nsets = max(2, min(4096, -(-int(2.5 * l2) // per_set)))
+            g = torch.Generator(device="cuda")
+            g.manual_seed(900 + M * 16 + N)
+            rnd = lambda *shape: torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)  # noqa: E731
+            P, A, A2 = rnd(nsets, M, H), rnd(nsets, M, H), rnd(nsets, M, H)
+            B = rnd(nsets, N, M, H)
+            w = (rnd(H) / H ** 0.5).to(torch.bfloat16)
+            gam = (1 + 0.1 * rnd(H).float()).to(torch.bfloat16)
+            O = torch.empty_like(P)
+            NP = torch.empty_like(P)
 
-            def call():
-                binding.attnres_add_rmsnorm(inp.prefix, inp.add, inp.add2, inp.bank, inp.w, inp.gamma,
-                                            inp.eps, out, newp, stream=s, check=False)
-            with torch.cuda.stream(s):
-                for _ in range(5):
-                    call()
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=s):
-                for _ in range(reps):
-                    call()
-            g.replay()
-            torch.cuda.synchronize()
-            warm = []
-            for _ in range(graph_replays):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(s)
-                g.replay()
-                e1.record(s)
-                e1.synchronize()
-                warm.append(e0.elapsed_time(e1) * 1e3 / reps)
-            cold = []
-            with torch.cuda.stream(s):
-                for _ in range(30):
-                    flush.fill_(1)
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(s)
-                    call()
-                    e1.record(s)
+            def call(i):
+                binding.attnres_add_rmsnorm(P[i], A[i], A2[i], B[i], w, gam, 1e-6, O[i], NP[i],
+                                            stream=s, check=False)
+
+            def timed(graph, calls):
+                out = []
+                for _ in range(replays):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    with torch.cuda.stream(s):
+                        e0.record(s)
+                        graph.replay()
+                        e1.record(s)
                     e1.synchronize()
-                    cold.append(e0.elapsed_time(e1) * 1e3)
-            del g
-            res[f"M{M}_N{N}"] = {"warm_us": round(statistics.median(warm), 3),
-                                 "cold_us": round(statistics.median(cold), 3),
-                                 "plan": binding.attnres_plan(M, N, H)}
-    del flush
-    torch.cuda.synchronize()
+                    out.append(e0.elapsed_time(e1) * 1e3 / calls)
+                return round(statistics.median(out), 3)
+
+            with torch.cuda.stream(s):
+                for i in range(min(nsets, 8)):
+                    call(i)
+            torch.cuda.synchronize()
+            gw = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gw, stream=s):
+                for _ in range(reps):
+                    call(0)
+            gc = torch.cuda.CUDAGraph()
+            ncold = max(reps, nsets)
+            with torch.cuda.graph(gc, stream=s):
+                for k in range(ncold):
+                    call(k % nsets)
+            with torch.cuda.stream(s):
+                gw.replay()
+                gc.replay()
+            torch.cuda.synchronize()
+            res[f"M{M}_N{N}"] = {"warm_us": timed(gw, reps), "cold_us": timed(gc, ncold),
+                                 "cold_sets": nsets,
+                                 "cluster": binding.attnres_plan(M, N, H)["cluster"]}
+            del gw, gc, P, A, A2, B, O, NP
+            torch.cuda.synchronize()
     return res
 
 
-def run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_over_ranks, ws):
+def run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_ranks, ws):
     """The same metric through the public API with pinned host buffers: every
     step copies the inputs host->device, calls the op, and copies both
     outputs back, all on the launching stream inside the timed region."""
@@ -334,8 +370,8 @@ def run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_over_ran
             e2e_step()
     e1.record(stream)
     barrier()
-    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3)
-    e2e_value = nbytes * ws * args.steps / e2e_s / 1e9
+    e2e_s = max_ranks(e0.elapsed_time(e1) / 1e3)
+    e2e_value = weak_scaling_value(nbytes, ws, args.steps, e2e_s)
     del dev, host, out_h, newp_h
     return {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s / args.steps * 1e3, 3)}
@@ -362,16 +398,12 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x):
-        if ws == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def max_ranks(x):
+        return max_over_ranks(x, "cuda")
 
     # ---- the bandwidth workload, resident in HBM
     M = args.tokens
-    inp = wl.bandwidth_inputs(device="cuda", seed=4 + rank, M=M)
+    inp = wl.bandwidth_inputs(device="cuda", seed=rank_seed(rank), M=M)
     stream = torch.cuda.Stream()
     call, ev, t0, t1, out, newp = time_bandwidth(binding, inp, args.steps, args.warmup, stream)
     nbytes = algorithmic_bytes(M, N_BW, H)
@@ -398,14 +430,14 @@ def run_ours(args):
     clocks = sampler.stop()
     total_s = t0.elapsed_time(t1) / 1e3
     launch_s = [a.elapsed_time(b) / 1e3 for a, b in ev]
-    total_s = max_over_ranks(total_s)
-    avg_launch = max_over_ranks(sum(launch_s) / len(launch_s))
-    value = nbytes * ws * args.steps / total_s / 1e9
+    total_s = max_ranks(total_s)
+    avg_launch = max_ranks(sum(launch_s) / len(launch_s))
+    value = weak_scaling_value(nbytes, ws, args.steps, total_s)
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_over_ranks, ws)
+        e2e = run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_ranks, ws)
 
     decode = None
     cpu_base = None

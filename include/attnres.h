@@ -102,15 +102,19 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
 /*
  * Launch configuration, for tests and benchmarks that pin one.
  *   variant   0 = automatic (same as attnres_add_rmsnorm);
- *             1 = one CTA per token, 16 columns per thread;
+ *             1 = one CTA per token, 16 columns per thread (<= 448 threads);
  *             2 = a thread-block cluster of `cluster` CTAs per token, each
  *                 CTA owning a contiguous 1/cluster of the columns, 8 columns
- *                 per thread; the per-token sums are exchanged through
- *                 distributed shared memory.
- *   cluster   CTAs per token for variant 2 (1..16); 0 = automatic.
- *   threads   threads per CTA (multiple of 32, up to 1024; for variant 2 at
- *             most 256 and cluster * threads/32 <= 32); 0 = the smallest
- *             count that covers the CTA's columns.
+ *                 per thread (<= 256 threads); the per-token sums are
+ *                 exchanged through distributed shared memory;
+ *             3 = as 2 with at most 224 threads and registers capped so that
+ *                 three CTAs share an SM (the large-M streaming shape).
+ *             All variants give bit-identical new_prefix; out is identical
+ *             for the same variant family and cluster size.
+ *   cluster   CTAs per token for variants 2 and 3 (1..16); 0 = the
+ *             smallest that fits the variant's thread limit.
+ *   threads   threads per CTA, a multiple of 32 within the variant's limit;
+ *             0 = the smallest count that covers the CTA's columns.
  *   grid_tokens  CTAs (clusters) along the token axis, each looping over
  *             tokens with this stride; 0 = min(M, 65535).
  */

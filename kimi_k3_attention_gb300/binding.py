@@ -19,7 +19,7 @@ STATUS = {
     -4: "ATTNRES_ERR_ALIAS", -5: "ATTNRES_ERR_EPS", -6: "ATTNRES_ERR_CUDA",
     -7: "ATTNRES_ERR_DEVICE", -8: "ATTNRES_ERR_CONFIG",
 }
-VARIANTS = {"auto": 0, "cta": 1, "cluster": 2}
+VARIANTS = {"auto": 0, "cta": 1, "cluster": 2, "stream": 3}
 
 # Every symbol include/attnres.h declares.
 EXPORTS = (

@@ -86,21 +86,25 @@ int round_up32(int x) { return (x + 31) & ~31; }
 // check the result.  Returns ATTNRES_OK or ATTNRES_ERR_CONFIG.
 int resolve(int M, int H, int sms, attnres_config* c) {
   const int H8 = H / 8;
+  auto min_cluster = [&](int maxt) {
+    int cl = 1;
+    while (cl <= 16 && round_up32((H8 + cl - 1) / cl) > maxt) ++cl;
+    return cl;
+  };
   if (c->variant == 0) {
-    c->variant = 2;
-    if (c->cluster == 0) {
-      // Latency regime: spread each token over enough CTAs that M * cluster
-      // covers the SMs; streaming regime: the smallest cluster whose CTAs
-      // fit the split shape, so several tokens are in flight per SM.
-      int cl = 1;
-      while (round_up32((H8 + cl - 1) / cl) > kSplitMaxT) ++cl;
-      if (M <= 64) {
+    // Latency regime (M <= 64): spread each token over enough CTAs that
+    // M * cluster covers the SMs.  Streaming regime: the smallest cluster
+    // whose CTAs fit the occupancy-capped shape, so that several tokens are
+    // in flight on every SM.
+    if (M > 64 && min_cluster(kStreamMaxT) <= 16) {
+      c->variant = 3;
+    } else {
+      c->variant = 2;
+      if (c->cluster == 0) {
+        int cl = min_cluster(kSplitMaxT);
         while (cl < 16 && M * cl < sms) cl *= 2;
-        if (cl > 16) cl = 16;
-      } else if (cl < 4 && round_up32((H8 + 3) / 4) <= kSplitMaxT && H8 >= 4 * 64) {
-        cl = 4;
+        c->cluster = cl > 16 ? 16 : cl;
       }
-      c->cluster = cl;
     }
   }
   if (c->variant == 1) {
@@ -110,17 +114,14 @@ int resolve(int M, int H, int sms, attnres_config* c) {
     if (c->threads == 0) c->threads = need;
     if (c->threads < need || c->threads > kCtaMaxT || (c->threads % 32) != 0)
       return ATTNRES_ERR_CONFIG;
-  } else if (c->variant == 2) {
-    if (c->cluster == 0) {
-      int cl = 1;
-      while (round_up32((H8 + cl - 1) / cl) > kSplitMaxT) ++cl;
-      c->cluster = cl;
-    }
+  } else if (c->variant == 2 || c->variant == 3) {
+    const int maxt = (c->variant == 2) ? kSplitMaxT : kStreamMaxT;
+    if (c->cluster == 0) c->cluster = min_cluster(maxt);
     if (c->cluster < 1 || c->cluster > 16) return ATTNRES_ERR_CONFIG;
     const int cpc = (H8 + c->cluster - 1) / c->cluster;
-    const int need = round_up32((cpc + kSplitVPT - 1) / kSplitVPT);
+    const int need = round_up32(cpc);
     if (c->threads == 0) c->threads = need;
-    if (c->threads < need || c->threads > kSplitMaxT || (c->threads % 32) != 0)
+    if (c->threads < need || c->threads > maxt || (c->threads % 32) != 0)
       return ATTNRES_ERR_CONFIG;
   } else {
     return ATTNRES_ERR_CONFIG;
@@ -130,12 +131,12 @@ int resolve(int M, int H, int sms, attnres_config* c) {
   return ATTNRES_OK;
 }
 
-template <int VPT, int MAXT>
+template <int VPT, int MAXT, int MINB>
 cudaError_t dispatch(int N, bool add2, const Params& p, dim3 g, int t, int c, cudaStream_t s) {
 #define ATTNRES_CASE(n)                                                          \
   case n:                                                                        \
-    return add2 ? launch_fused<n, true, VPT, MAXT>(p, g, t, c, s)                \
-                : launch_fused<n, false, VPT, MAXT>(p, g, t, c, s);
+    return add2 ? launch_fused<n, true, VPT, MAXT, MINB>(p, g, t, c, s)          \
+                : launch_fused<n, false, VPT, MAXT, MINB>(p, g, t, c, s);
   switch (N) {
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
     ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
@@ -182,9 +183,13 @@ extern "C" int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const
   const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool has_add2 = add2 != nullptr;
-  cudaError_t e = (c.variant == 1)
-                      ? dispatch<kCtaVPT, kCtaMaxT>(N, has_add2, p, grid, c.threads, 1, s)
-                      : dispatch<kSplitVPT, kSplitMaxT>(N, has_add2, p, grid, c.threads, c.cluster, s);
+  cudaError_t e;
+  if (c.variant == 1)
+    e = dispatch<kCtaVPT, kCtaMaxT, kCtaMinB>(N, has_add2, p, grid, c.threads, 1, s);
+  else if (c.variant == 2)
+    e = dispatch<kSplitVPT, kSplitMaxT, kSplitMinB>(N, has_add2, p, grid, c.threads, c.cluster, s);
+  else
+    e = dispatch<kStreamVPT, kStreamMaxT, kStreamMinB>(N, has_add2, p, grid, c.threads, c.cluster, s);
   if (e != cudaSuccess) return fail_cuda(e);
   return ATTNRES_OK;
 }

@@ -146,6 +146,10 @@ __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -216,8 +220,8 @@ struct Pow2 {
 
 // ---------------------------------------------------------------- the kernel
 
-template <int N, bool ADD2, int VPT, int MAXT>
-__global__ void __launch_bounds__(MAXT) attnres_fused_kernel(const Params p) {
+template <int N, bool ADD2, int VPT, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params p) {
   constexpr int S = N + 1;             // sources: bank[0..N-1], new prefix
   constexpr int K = 2 * S;             // per-token sums: (ss_i, d_i)
   constexpr int KP = Pow2<K>::value;
@@ -265,12 +269,10 @@ __global__ void __launch_bounds__(MAXT) attnres_fused_kernel(const Params p) {
         v[i][k] = ok[k] ? ld_stream(p.bank + i * p.bank_stride + row + jj[k]) : z;
     }
 
-    // ---- fold, store the updated prefix
+    // ---- fold (the updated prefix is stored at the end: a global store in
+    // flight would make every release barrier below wait for it)
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      v[N][k] = fold_chunk<ADD2>(pr[k], ad[k], ad2[k]);
-      if (ok[k]) st_out(p.new_prefix + row + jj[k], v[N][k]);
-    }
+    for (int k = 0; k < VPT; ++k) v[N][k] = fold_chunk<ADD2>(pr[k], ad[k], ad2[k]);
 
     // ---- per-source sums of squares and dot products with w
     float part[KP];
@@ -355,13 +357,16 @@ __global__ void __launch_bounds__(MAXT) attnres_fused_kernel(const Params p) {
     for (int idx = lane; idx < nw_total; idx += 32)
       qq += ld_dsmem(dsmem_addr(&red2[idx % nwarps], static_cast<uint32_t>(idx / nwarps)));
     qq = warp_sum(qq);
-    cluster_arrive();  // this CTA is done reading the cluster's shared memory
+    // This CTA has consumed every remote value it reads for this token; the
+    // arrive orders nothing else, so it can be relaxed.
+    cluster_arrive_relaxed();
     const float rh = rsqrtf(__fmaf_rn(qq, p.inv_h, p.eps));
 
-    // ---- output
+    // ---- outputs
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       if (ok[k]) {
+        st_out(p.new_prefix + row + jj[k], v[N][k]);
         uint4 o;
         o.x = pack_bf16x2(mul_rn(mul_rn(h[k][0], rh), elem(gv[k], 0)),
                           mul_rn(mul_rn(h[k][1], rh), elem(gv[k], 1)));
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(MAXT) attnres_fused_kernel(const Params p) {
 }
 
 // Host-side launcher of one instantiation (defined in attnres_launch.cuh).
-template <int N, bool ADD2, int VPT, int MAXT>
+template <int N, bool ADD2, int VPT, int MAXT, int MINB>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, cudaStream_t s);
 
 }  // namespace attnres

@@ -10,15 +10,18 @@ namespace attnres {
 
 constexpr int kMaxDevices = 64;
 
-// The two compiled shapes of the kernel.
-//   split: 8 columns per thread, up to 256 threads (cluster of CTAs per token)
-//   cta:   16 columns per thread, up to 448 threads (one CTA per token)
-constexpr int kSplitVPT = 1, kSplitMaxT = 256;
-constexpr int kCtaVPT = 2, kCtaMaxT = 448;
+// The compiled shapes of the kernel.
+//   split:  8 columns per thread, up to 256 threads (a cluster of CTAs per token)
+//   stream: 8 columns per thread, up to 224 threads, registers capped so
+//           that three CTAs fit an SM (many tokens in flight at large M)
+//   cta:    16 columns per thread, up to 448 threads (one CTA per token)
+constexpr int kSplitVPT = 1, kSplitMaxT = 256, kSplitMinB = 1;
+constexpr int kStreamVPT = 1, kStreamMaxT = 224, kStreamMinB = 3;
+constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 
-template <int N, bool ADD2, int VPT, int MAXT>
+template <int N, bool ADD2, int VPT, int MAXT, int MINB>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, cudaStream_t s) {
-  auto kern = attnres_fused_kernel<N, ADD2, VPT, MAXT>;
+  auto kern = attnres_fused_kernel<N, ADD2, VPT, MAXT, MINB>;
   // Cluster sizes above 8 need an opt-in per function and device.
   static std::atomic<unsigned char> opted[kMaxDevices];
   if (cluster > 8) {
@@ -47,10 +50,12 @@ cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, c
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-#define ATTNRES_INSTANTIATE(N, ADD2)                                                        \
-  template cudaError_t launch_fused<N, ADD2, kSplitVPT, kSplitMaxT>(const Params&, dim3, int, \
-                                                                     int, cudaStream_t);      \
-  template cudaError_t launch_fused<N, ADD2, kCtaVPT, kCtaMaxT>(const Params&, dim3, int, int, \
-                                                                 cudaStream_t);
+#define ATTNRES_INSTANTIATE(N, ADD2)                                                       \
+  template cudaError_t launch_fused<N, ADD2, kSplitVPT, kSplitMaxT, kSplitMinB>(             \
+      const Params&, dim3, int, int, cudaStream_t);                                          \
+  template cudaError_t launch_fused<N, ADD2, kStreamVPT, kStreamMaxT, kStreamMinB>(          \
+      const Params&, dim3, int, int, cudaStream_t);                                          \
+  template cudaError_t launch_fused<N, ADD2, kCtaVPT, kCtaMaxT, kCtaMinB>(const Params&, dim3, \
+                                                                          int, int, cudaStream_t);
 
 }  // namespace attnres

@@ -65,13 +65,17 @@ def _ceil(a, b):
 
 def split_configs(H):
     """Every cluster size whose CTAs fit the split shape (<= 256 threads of 8
-    columns) for this H, the one-CTA-per-token variant where it fits (<= 448
-    threads of 16 columns), and the automatic choice (None)."""
+    columns) or the streaming shape (<= 224 threads) for this H, the
+    one-CTA-per-token variant where it fits (<= 448 threads of 16 columns),
+    and the automatic choice (None)."""
     H8 = H // 8
     cfgs = [None]
     for c in range(1, 17):
         if _ceil(_ceil(H8, c), 32) * 32 <= 256:
             cfgs.append(binding.make_config("cluster", cluster=c))
+    for c in range(1, 17):
+        if _ceil(_ceil(H8, c), 32) * 32 <= 224:
+            cfgs.append(binding.make_config("stream", cluster=c))
     if _ceil(_ceil(H8, 2), 32) * 32 <= 448:
         cfgs.append(binding.make_config("cta"))
     return cfgs
@@ -81,4 +85,6 @@ def cfg_name(c):
     if c is None:
         return "auto"
     d = c.as_dict()
-    return "cta" if d["variant"] == 1 else f"cluster{d['cluster']}"
+    if d["variant"] == 1:
+        return "cta"
+    return f"{'cluster' if d['variant'] == 2 else 'stream'}{d['cluster']}"

@@ -57,6 +57,7 @@ def test_decode_every_variant(cfg, M, N):
 
 @pytest.mark.parametrize("special_prefix", [False, True])
 @pytest.mark.parametrize("cfg", [None, binding.make_config("cluster", cluster=4),
+                                 binding.make_config("stream", cluster=4),
                                  binding.make_config("cta")], ids=cfg_name)
 def test_bit_exact_stress(special_prefix, cfg):
     inp = wl.stress_inputs(special_prefix=special_prefix)
@@ -229,8 +230,8 @@ def test_ragged_and_small_hidden_sizes(Hs):
 def test_token_loop(grid_tokens):
     """Fewer token CTAs than tokens: each cluster loops over tokens."""
     inp = wl.make_inputs(67, 6, H, seed=11)
-    for cl in (4, 8):
-        cfg = binding.make_config("cluster", cluster=cl, grid_tokens=grid_tokens)
+    for variant, cl in (("cluster", 4), ("cluster", 8), ("stream", 4)):
+        cfg = binding.make_config(variant, cluster=cl, grid_tokens=grid_tokens)
         gnp, gout = run_gpu(inp, cfg)
         assert_parity(inp, gnp, gout)
     gnp, gout = run_gpu(inp, binding.make_config("cta", grid_tokens=grid_tokens))
