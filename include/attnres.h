@@ -117,12 +117,18 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *             0 = the smallest count that covers the CTA's columns.
  *   grid_tokens  CTAs (clusters) along the token axis, each looping over
  *             tokens with this stride; 0 = min(M, 65535).
+ *   pdl       programmatic dependent launch: 1 = on, -1 = off, 0 = the
+ *             default (on).  With it the kernel may be scheduled while the
+ *             previous kernel on the stream is still running; it waits for
+ *             that kernel to complete before its first global-memory access,
+ *             so results are the same either way.
  */
 typedef struct {
   int variant;
   int cluster;
   int threads;
   int grid_tokens;
+  int pdl;
 } attnres_config;
 
 /* The fused epilogue with a pinned configuration (cfg may be NULL = auto).
@@ -134,7 +140,7 @@ int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const void* add2
                            const attnres_config* cfg);
 
 /* The configuration attnres_add_rmsnorm would launch for (M, N, H) on the
- * current device, written to *plan (all four fields resolved).  Returns a
+ * current device, written to *plan (every field resolved).  Returns a
  * status; needs a CUDA device (it reads the SM count). */
 int attnres_plan(int M, int N, int H, attnres_config* plan);
 

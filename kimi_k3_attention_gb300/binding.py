@@ -40,7 +40,7 @@ class AttnResError(RuntimeError):
 
 class Config(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("cluster", ctypes.c_int),
-                ("threads", ctypes.c_int), ("grid_tokens", ctypes.c_int)]
+                ("threads", ctypes.c_int), ("grid_tokens", ctypes.c_int), ("pdl", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -101,9 +101,9 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def make_config(variant="auto", cluster=0, threads=0, grid_tokens=0) -> Config:
+def make_config(variant="auto", cluster=0, threads=0, grid_tokens=0, pdl=0) -> Config:
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
-    return Config(v, int(cluster), int(threads), int(grid_tokens))
+    return Config(v, int(cluster), int(threads), int(grid_tokens), int(pdl))
 
 
 def _check_tensor(name, t, shape=None):

@@ -128,15 +128,18 @@ int resolve(int M, int H, int sms, attnres_config* c) {
   }
   if (c->grid_tokens == 0) c->grid_tokens = M < 65535 ? M : 65535;
   if (c->grid_tokens < 1 || c->grid_tokens > 65535) return ATTNRES_ERR_CONFIG;
+  if (c->pdl < -1 || c->pdl > 1) return ATTNRES_ERR_CONFIG;
+  if (c->pdl == 0) c->pdl = 1;
   return ATTNRES_OK;
 }
 
 template <int VPT, int MAXT, int MINB>
-cudaError_t dispatch(int N, bool add2, const Params& p, dim3 g, int t, int c, cudaStream_t s) {
+cudaError_t dispatch(int N, bool add2, const Params& p, dim3 g, int t, int c, bool pdl,
+                     cudaStream_t s) {
 #define ATTNRES_CASE(n)                                                          \
   case n:                                                                        \
-    return add2 ? launch_fused<n, true, VPT, MAXT, MINB>(p, g, t, c, s)          \
-                : launch_fused<n, false, VPT, MAXT, MINB>(p, g, t, c, s);
+    return add2 ? launch_fused<n, true, VPT, MAXT, MINB>(p, g, t, c, pdl, s)     \
+                : launch_fused<n, false, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
   switch (N) {
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
     ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
@@ -161,7 +164,7 @@ extern "C" int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const
   if (st != ATTNRES_OK) return st;
   int sms = 0;
   if ((st = current_device(&sms)) != ATTNRES_OK) return st;
-  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0};
+  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0};
   if ((st = resolve(M, H, sms, &c)) != ATTNRES_OK) return st;
 
   Params p;
@@ -183,13 +186,16 @@ extern "C" int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const
   const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool has_add2 = add2 != nullptr;
+  const bool pdl = c.pdl >= 0;
   cudaError_t e;
   if (c.variant == 1)
-    e = dispatch<kCtaVPT, kCtaMaxT, kCtaMinB>(N, has_add2, p, grid, c.threads, 1, s);
+    e = dispatch<kCtaVPT, kCtaMaxT, kCtaMinB>(N, has_add2, p, grid, c.threads, 1, pdl, s);
   else if (c.variant == 2)
-    e = dispatch<kSplitVPT, kSplitMaxT, kSplitMinB>(N, has_add2, p, grid, c.threads, c.cluster, s);
+    e = dispatch<kSplitVPT, kSplitMaxT, kSplitMinB>(N, has_add2, p, grid, c.threads, c.cluster,
+                                                    pdl, s);
   else
-    e = dispatch<kStreamVPT, kStreamMaxT, kStreamMinB>(N, has_add2, p, grid, c.threads, c.cluster, s);
+    e = dispatch<kStreamVPT, kStreamMaxT, kStreamMinB>(N, has_add2, p, grid, c.threads,
+                                                       c.cluster, pdl, s);
   if (e != cudaSuccess) return fail_cuda(e);
   return ATTNRES_OK;
 }
@@ -209,7 +215,7 @@ extern "C" int attnres_plan(int M, int N, int H, attnres_config* plan) {
   int sms = 0;
   int st = current_device(&sms);
   if (st != ATTNRES_OK) return st;
-  attnres_config c = {0, 0, 0, 0};
+  attnres_config c = {0, 0, 0, 0, 0};
   if ((st = resolve(M, H, sms, &c)) != ATTNRES_OK) return st;
   *plan = c;
   return ATTNRES_OK;

@@ -130,6 +130,14 @@ __device__ __forceinline__ uint4 fold_chunk(const uint4& p, const uint4& a, cons
   return r;
 }
 
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -248,6 +256,12 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     ok[k] = jj[k] < cend;
   }
 
+  // Programmatic dependent launch: this grid may have been scheduled while
+  // the previous kernel on the stream was still running; wait for it to
+  // complete (and its writes to be visible) before touching global memory.
+  // Without the launch attribute this returns at once.
+  griddep_wait();
+
   uint4 wv[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) wv[k] = ok[k] ? ld_keep(p.w + jj[k]) : make_uint4(0, 0, 0, 0);
@@ -268,6 +282,10 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
       for (int i = 0; i < N; ++i)
         v[i][k] = ok[k] ? ld_stream(p.bank + i * p.bank_stride + row + jj[k]) : z;
     }
+
+    // Let the next kernel on the stream be scheduled once every CTA of this
+    // grid is past its loads; it still waits for this grid to finish.
+    griddep_launch_dependents();
 
     // ---- fold (the updated prefix is stored at the end: a global store in
     // flight would make every release barrier below wait for it)
@@ -387,6 +405,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
 
 // Host-side launcher of one instantiation (defined in attnres_launch.cuh).
 template <int N, bool ADD2, int VPT, int MAXT, int MINB>
-cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, cudaStream_t s);
+cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
+                         cudaStream_t s);
 
 }  // namespace attnres

@@ -20,7 +20,8 @@ constexpr int kStreamVPT = 1, kStreamMaxT = 224, kStreamMinB = 3;
 constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 
 template <int N, bool ADD2, int VPT, int MAXT, int MINB>
-cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, cudaStream_t s) {
+cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
+                         cudaStream_t s) {
   auto kern = attnres_fused_kernel<N, ADD2, VPT, MAXT, MINB>;
   // Cluster sizes above 8 need an opt-in per function and device.
   static std::atomic<unsigned char> opted[kMaxDevices];
@@ -40,22 +41,24 @@ cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, c
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 #define ATTNRES_INSTANTIATE(N, ADD2)                                                       \
   template cudaError_t launch_fused<N, ADD2, kSplitVPT, kSplitMaxT, kSplitMinB>(             \
-      const Params&, dim3, int, int, cudaStream_t);                                          \
+      const Params&, dim3, int, int, bool, cudaStream_t);                                    \
   template cudaError_t launch_fused<N, ADD2, kStreamVPT, kStreamMaxT, kStreamMinB>(          \
-      const Params&, dim3, int, int, cudaStream_t);                                          \
-  template cudaError_t launch_fused<N, ADD2, kCtaVPT, kCtaMaxT, kCtaMinB>(const Params&, dim3, \
-                                                                          int, int, cudaStream_t);
+      const Params&, dim3, int, int, bool, cudaStream_t);                                    \
+  template cudaError_t launch_fused<N, ADD2, kCtaVPT, kCtaMaxT, kCtaMinB>(                   \
+      const Params&, dim3, int, int, bool, cudaStream_t);
 
 }  // namespace attnres
