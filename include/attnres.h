@@ -108,7 +108,12 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *                 per thread (<= 256 threads); the per-token sums are
  *                 exchanged through distributed shared memory;
  *             3 = as 2 with at most 224 threads and registers capped so that
- *                 three CTAs share an SM (the large-M streaming shape).
+ *                 three CTAs share an SM;
+ *             4 = persistent and pipelined (the large-M streaming kernel): a
+ *                 grid of as many clusters as fit the GPU at once walks the
+ *                 tokens; every thread copies its chunks of the token
+ *                 `stages`-1 steps ahead into a shared-memory ring (cp.async),
+ *                 so HBM reads continue during the reductions.
  *             All variants give bit-identical new_prefix; out is identical
  *             for the same variant family and cluster size.
  *   cluster   CTAs per token for variants 2 and 3 (1..16); 0 = the
@@ -116,12 +121,16 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *   threads   threads per CTA, a multiple of 32 within the variant's limit;
  *             0 = the smallest count that covers the CTA's columns.
  *   grid_tokens  CTAs (clusters) along the token axis, each looping over
- *             tokens with this stride; 0 = min(M, 65535).
+ *             tokens with this stride; 0 = min(M, 65535), or for variant 4
+ *             the number of clusters that can be resident at once.
  *   pdl       programmatic dependent launch: 1 = on, -1 = off, 0 = the
  *             default (on).  With it the kernel may be scheduled while the
  *             previous kernel on the stream is still running; it waits for
  *             that kernel to complete before its first global-memory access,
  *             so results are the same either way.
+ *   stages    variant 4 only: tokens held by the shared-memory ring (2..4);
+ *             0 = as many as fit 227 KB of shared memory.  Must be 0 for
+ *             the other variants.
  */
 typedef struct {
   int variant;
@@ -129,6 +138,7 @@ typedef struct {
   int threads;
   int grid_tokens;
   int pdl;
+  int stages;
 } attnres_config;
 
 /* The fused epilogue with a pinned configuration (cfg may be NULL = auto).
@@ -139,10 +149,12 @@ int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const void* add2
                            int M, int N, int H, attnres_stream_t stream,
                            const attnres_config* cfg);
 
-/* The configuration attnres_add_rmsnorm would launch for (M, N, H) on the
- * current device, written to *plan (every field resolved).  Returns a
- * status; needs a CUDA device (it reads the SM count). */
-int attnres_plan(int M, int N, int H, attnres_config* plan);
+/* The configuration attnres_add_rmsnorm would launch for (M, N, H) with
+ * (has_add2 != 0) or without a second addend on the current device, written
+ * to *plan with every field resolved (grid_tokens 0 for variant 4 means
+ * "as many clusters as fit").  Returns a status; needs a CUDA device (it
+ * reads the SM count). */
+int attnres_plan(int M, int N, int H, int has_add2, attnres_config* plan);
 
 /* Static description of a status code; never NULL. */
 const char* attnres_status_string(int status);

@@ -19,7 +19,7 @@ STATUS = {
     -4: "ATTNRES_ERR_ALIAS", -5: "ATTNRES_ERR_EPS", -6: "ATTNRES_ERR_CUDA",
     -7: "ATTNRES_ERR_DEVICE", -8: "ATTNRES_ERR_CONFIG",
 }
-VARIANTS = {"auto": 0, "cta": 1, "cluster": 2, "stream": 3}
+VARIANTS = {"auto": 0, "cta": 1, "cluster": 2, "stream": 3, "pipe": 4}
 
 # Every symbol include/attnres.h declares.
 EXPORTS = (
@@ -40,7 +40,8 @@ class AttnResError(RuntimeError):
 
 class Config(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("cluster", ctypes.c_int),
-                ("threads", ctypes.c_int), ("grid_tokens", ctypes.c_int), ("pdl", ctypes.c_int)]
+                ("threads", ctypes.c_int), ("grid_tokens", ctypes.c_int), ("pdl", ctypes.c_int),
+                ("stages", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -64,7 +65,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attnres_add_rmsnorm.restype = i
     lib.attnres_add_rmsnorm_ex.argtypes = args + [ctypes.POINTER(Config)]
     lib.attnres_add_rmsnorm_ex.restype = i
-    lib.attnres_plan.argtypes = [i, i, i, ctypes.POINTER(Config)]
+    lib.attnres_plan.argtypes = [i, i, i, i, ctypes.POINTER(Config)]
     lib.attnres_plan.restype = i
     lib.attnres_status_string.argtypes = [i]
     lib.attnres_status_string.restype = ctypes.c_char_p
@@ -101,9 +102,9 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def make_config(variant="auto", cluster=0, threads=0, grid_tokens=0, pdl=0) -> Config:
+def make_config(variant="auto", cluster=0, threads=0, grid_tokens=0, pdl=0, stages=0) -> Config:
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
-    return Config(v, int(cluster), int(threads), int(grid_tokens), int(pdl))
+    return Config(v, int(cluster), int(threads), int(grid_tokens), int(pdl), int(stages))
 
 
 def _check_tensor(name, t, shape=None):
@@ -160,9 +161,9 @@ def attnres_add_rmsnorm_raw(prefix, add, add2, bank, w, gamma, eps, out, new_pre
     return lib.attnres_add_rmsnorm_ex(*args, ctypes.byref(config))
 
 
-def attnres_plan(M, N, H) -> dict:
+def attnres_plan(M, N, H, has_add2=True) -> dict:
     c = Config()
-    _check(load().attnres_plan(int(M), int(N), int(H), ctypes.byref(c)))
+    _check(load().attnres_plan(int(M), int(N), int(H), int(bool(has_add2)), ctypes.byref(c)))
     return c.as_dict()
 
 

@@ -84,7 +84,11 @@ int round_up32(int x) { return (x + 31) & ~31; }
 
 // Fill every zero field of *c for (M, H) on a device with `sms` SMs, then
 // check the result.  Returns ATTNRES_OK or ATTNRES_ERR_CONFIG.
-int resolve(int M, int H, int sms, attnres_config* c) {
+// Dynamic shared memory the pipelined ring may take: the 227 KB a CTA can
+// hold, less the kernel's static exchange buffers and a little slack.
+constexpr size_t kPipeSmemMax = 227 * 1024 - sizeof(Exchange) - 1024;
+
+int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
   const int H8 = H / 8;
   auto min_cluster = [&](int maxt) {
     int cl = 1;
@@ -96,8 +100,8 @@ int resolve(int M, int H, int sms, attnres_config* c) {
     // M * cluster covers the SMs.  Streaming regime: the smallest cluster
     // whose CTAs fit the occupancy-capped shape, so that several tokens are
     // in flight on every SM.
-    if (M > 64 && min_cluster(kStreamMaxT) <= 16) {
-      c->variant = 3;
+    if (M > 64 && min_cluster(kPipeMaxT) <= 16) {
+      c->variant = 4;
     } else {
       c->variant = 2;
       if (c->cluster == 0) {
@@ -123,11 +127,33 @@ int resolve(int M, int H, int sms, attnres_config* c) {
     if (c->threads == 0) c->threads = need;
     if (c->threads < need || c->threads > maxt || (c->threads % 32) != 0)
       return ATTNRES_ERR_CONFIG;
+  } else if (c->variant == 4) {
+    if (c->cluster == 0) c->cluster = min_cluster(kPipeMaxT);
+    if (c->cluster < 1 || c->cluster > 16) return ATTNRES_ERR_CONFIG;
+    const int cpc = (H8 + c->cluster - 1) / c->cluster;
+    const int need = round_up32(cpc);
+    if (c->threads == 0) c->threads = need;
+    if (c->threads < need || c->threads > kPipeMaxT || (c->threads % 32) != 0)
+      return ATTNRES_ERR_CONFIG;
+    if (c->stages == 0) {
+      c->stages = 4;
+      while (c->stages > 2 && pipe_smem_bytes(N, add2, c->threads, c->stages) > kPipeSmemMax)
+        --c->stages;
+    }
+    if (c->stages < 2 || c->stages > 4 ||
+        pipe_smem_bytes(N, add2, c->threads, c->stages) > kPipeSmemMax)
+      return ATTNRES_ERR_CONFIG;
+    // grid_tokens 0 stays 0: the launcher sizes the grid to the resident
+    // clusters.
+    if (c->grid_tokens < 0 || c->grid_tokens > 65535) return ATTNRES_ERR_CONFIG;
   } else {
     return ATTNRES_ERR_CONFIG;
   }
-  if (c->grid_tokens == 0) c->grid_tokens = M < 65535 ? M : 65535;
-  if (c->grid_tokens < 1 || c->grid_tokens > 65535) return ATTNRES_ERR_CONFIG;
+  if (c->variant != 4) {
+    if (c->stages != 0) return ATTNRES_ERR_CONFIG;
+    if (c->grid_tokens == 0) c->grid_tokens = M < 65535 ? M : 65535;
+    if (c->grid_tokens < 1 || c->grid_tokens > 65535) return ATTNRES_ERR_CONFIG;
+  }
   if (c->pdl < -1 || c->pdl > 1) return ATTNRES_ERR_CONFIG;
   if (c->pdl == 0) c->pdl = 1;
   return ATTNRES_OK;
@@ -140,6 +166,33 @@ cudaError_t dispatch(int N, bool add2, const Params& p, dim3 g, int t, int c, bo
   case n:                                                                        \
     return add2 ? launch_fused<n, true, VPT, MAXT, MINB>(p, g, t, c, pdl, s)     \
                 : launch_fused<n, false, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
+  switch (N) {
+    ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
+    ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
+    ATTNRES_CASE(9) ATTNRES_CASE(10) ATTNRES_CASE(11) ATTNRES_CASE(12)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef ATTNRES_CASE
+}
+
+template <int N, bool ADD2>
+cudaError_t dispatch_pipe_stages(int stages, const Params& p, dim3 g, int t, int c, bool pdl,
+                                 cudaStream_t s) {
+  switch (stages) {
+    case 2: return launch_pipe<N, ADD2, 2>(p, g, t, c, pdl, s);
+    case 3: return launch_pipe<N, ADD2, 3>(p, g, t, c, pdl, s);
+    case 4: return launch_pipe<N, ADD2, 4>(p, g, t, c, pdl, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t dispatch_pipe(int N, bool add2, int stages, const Params& p, dim3 g, int t, int c,
+                          bool pdl, cudaStream_t s) {
+#define ATTNRES_CASE(n)                                                              \
+  case n:                                                                            \
+    return add2 ? dispatch_pipe_stages<n, true>(stages, p, g, t, c, pdl, s)          \
+                : dispatch_pipe_stages<n, false>(stages, p, g, t, c, pdl, s);
   switch (N) {
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
     ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
@@ -164,8 +217,8 @@ extern "C" int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const
   if (st != ATTNRES_OK) return st;
   int sms = 0;
   if ((st = current_device(&sms)) != ATTNRES_OK) return st;
-  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0};
-  if ((st = resolve(M, H, sms, &c)) != ATTNRES_OK) return st;
+  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0, 0};
+  if ((st = resolve(M, N, add2 != nullptr, H, sms, &c)) != ATTNRES_OK) return st;
 
   Params p;
   p.prefix = static_cast<const uint4*>(prefix);
@@ -193,9 +246,11 @@ extern "C" int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const
   else if (c.variant == 2)
     e = dispatch<kSplitVPT, kSplitMaxT, kSplitMinB>(N, has_add2, p, grid, c.threads, c.cluster,
                                                     pdl, s);
-  else
+  else if (c.variant == 3)
     e = dispatch<kStreamVPT, kStreamMaxT, kStreamMinB>(N, has_add2, p, grid, c.threads,
                                                        c.cluster, pdl, s);
+  else
+    e = dispatch_pipe(N, has_add2, c.stages, p, grid, c.threads, c.cluster, pdl, s);
   if (e != cudaSuccess) return fail_cuda(e);
   return ATTNRES_OK;
 }
@@ -208,15 +263,15 @@ extern "C" int attnres_add_rmsnorm(const void* prefix, const void* add, const vo
                                 stream, nullptr);
 }
 
-extern "C" int attnres_plan(int M, int N, int H, attnres_config* plan) {
+extern "C" int attnres_plan(int M, int N, int H, int has_add2, attnres_config* plan) {
   if (!plan) return ATTNRES_ERR_NULL;
   if (M < 1 || N < 1 || N > ATTNRES_MAX_N || H < 8 || H > ATTNRES_MAX_H || (H % 8) != 0)
     return ATTNRES_ERR_SHAPE;
   int sms = 0;
   int st = current_device(&sms);
   if (st != ATTNRES_OK) return st;
-  attnres_config c = {0, 0, 0, 0, 0};
-  if ((st = resolve(M, H, sms, &c)) != ATTNRES_OK) return st;
+  attnres_config c = {0, 0, 0, 0, 0, 0};
+  if ((st = resolve(M, N, has_add2 != 0, H, sms, &c)) != ATTNRES_OK) return st;
   *plan = c;
   return ATTNRES_OK;
 }

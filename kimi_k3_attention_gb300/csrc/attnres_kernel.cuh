@@ -5,22 +5,28 @@
 // H/8 sixteen-byte chunks; every thread owns VPT chunks of every source row
 // and keeps them in registers from the single HBM read to the final store:
 //
-//   load    prefix, add, add2, bank[0..N-1] chunks (16-byte vector loads)
+//   load    prefix, add, add2, bank[0..N-1] chunks: 16-byte vector loads
+//           straight to registers (attnres_fused_kernel), or cp.async copies
+//           into a per-thread shared-memory ring several tokens ahead
+//           (attnres_pipe_kernel, persistent)
 //   fold    new_prefix = bf16(prefix + bf16(add + add2)) with add.rn.f32 and
 //           cvt.rn.bf16x2.f32 written in PTX, so no fast-math flag can turn
 //           them into flush-to-zero forms (TensorRT-LLM PR #20546, "Op")
 //   stats   ss_i = sum v^2 and d_i = w.v for the N+1 sources, one pass
 //   R1      2(N+1) partial sums: warp transpose-reduction, CTA sum in shared
-//           memory, cluster exchange through distributed shared memory
+//           memory, then every CTA pushes its totals into the shared memory
+//           of every CTA of the cluster (distributed shared memory) and one
+//           cluster barrier publishes them
 //   softmax every warp evaluates logits and softmax redundantly from the same
 //           totals in the same order, so all warps of all CTAs agree bitwise
 //   mix     h = sum_i alpha_i v_i from registers (no second read)
-//   R2      sum h^2: warp reduction, cluster exchange
-//   out     bf16(h * rsqrt(mean(h^2) + eps) * gamma)
+//   R2      sum h^2: warp reduction, pushed to every CTA, one cluster barrier
+//   out     bf16(h * rsqrt(mean(h^2) + eps) * gamma) and new_prefix stored
 //
 // Every reduction has a fixed order, so results are deterministic.  The
-// kernel has no spin-waits: the only waits are the hardware CTA and cluster
-// barriers, which every thread of every CTA reaches on the same path.
+// kernels have no spin-waits: the only waits are the hardware CTA and
+// cluster barriers, which every thread of every CTA reaches on the same path,
+// and cp.async.wait_group, which completes with the copies it waits for.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -167,19 +173,44 @@ __device__ __forceinline__ void cluster_sync() {
   cluster_wait();
 }
 
-// Address of the same shared-memory variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
-  const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+// Shared::cluster address of the same shared-memory location (given as a
+// shared::cta address) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
 }
 
-__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ void st_dsmem(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global -> shared copy, bypassing L1 (Ampere-style asynchronous copy).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int PENDING>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(addr));
+  return r;
+}
+
 
 // XOR-butterfly sums: every lane ends with the same bits, because each step
 // adds the same two operands (in either order) in every lane of a pair.
@@ -226,33 +257,218 @@ struct Pow2 {
   static constexpr int log2 = K <= 2 ? 1 : K <= 4 ? 2 : K <= 8 ? 3 : K <= 16 ? 4 : 5;
 };
 
-// ---------------------------------------------------------------- the kernel
+// ---------------------------------------------------------------- per token
 
-template <int N, bool ADD2, int VPT, int MAXT, int MINB>
-__global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params p) {
+// Shared memory of the per-token reductions.
+//   red:  per-warp partials of R1 (local)
+//   xin1: R1 totals pushed by each CTA of the cluster, indexed by its rank
+//   xin2: per-warp sums of h^2 pushed by each CTA, index rank * warps + warp
+// A CTA writes into a peer's xin1 only after the R2 barrier of the previous
+// token (which the peer passed after reading its xin1), and into xin2 only
+// after the R1 barrier of the same token (which the peer passed after
+// reading its xin2 of the previous token): two barriers per token, none at
+// exit, because no CTA touches another's shared memory after the R2 barrier.
+struct Exchange {
+  float red[32][32];
+  float xin1[16][32];
+  float xin2[512];
+};
+
+struct Thread {
+  int lane, warp, nwarps;
+  uint32_t crank, csize;
+};
+
+// Where a token's sources live between the two passes over them.
+//   RegSources:  all N+1 chunks in registers (loaded once from HBM).
+//   SmemSources: the N bank chunks in this thread's own slots of the
+//                shared-memory ring, read once per pass; the updated prefix
+//                in registers.
+template <int N, int VPT>
+struct RegSources {
+  uint4 (&v)[N + 1][VPT];
+  __device__ __forceinline__ uint4 get(int i, int k) const { return v[i][k]; }
+  __device__ __forceinline__ void set_new_prefix(int k, const uint4& u) { v[N][k] = u; }
+  __device__ __forceinline__ uint4 new_prefix(int k) const { return v[N][k]; }
+  // Keep only the packed BF16 words alive across the reductions: without
+  // this the compiler reuses the unpacked floats of the first pass in the
+  // mixture and holds twice the registers.
+  __device__ __forceinline__ void fence() {
+#pragma unroll
+    for (int i = 0; i <= N; ++i)
+#pragma unroll
+      for (int k = 0; k < VPT; ++k)
+        asm volatile("" : "+r"(v[i][k].x), "+r"(v[i][k].y), "+r"(v[i][k].z), "+r"(v[i][k].w));
+  }
+};
+
+template <int N>
+struct SmemSources {
+  uint32_t bank0;     // shared address of this thread's bank[0] slot
+  uint32_t step;      // bytes between consecutive rows of a stage
+  bool ok;
+  uint4 np;
+  __device__ __forceinline__ uint4 get(int i, int) const {
+    if (i == N) return np;
+    return ok ? lds16(bank0 + static_cast<uint32_t>(i) * step) : make_uint4(0, 0, 0, 0);
+  }
+  __device__ __forceinline__ void set_new_prefix(int, const uint4& u) { np = u; }
+  __device__ __forceinline__ uint4 new_prefix(int) const { return np; }
+  __device__ __forceinline__ void fence() {}
+};
+
+// Everything after the loads for one token: fold, sums, both exchanges,
+// softmax, mixture, and the two stores.  pr/ad/ad2 are the token's prefix and
+// addend chunks, src gives the bank chunks (and receives the updated prefix),
+// wv the pseudo-query chunks; masked chunks (ok false) are zeros and store
+// nothing.
+template <int N, bool ADD2, int VPT, class Src>
+__device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, const Thread& t,
+                                               size_t row, const int (&jj)[VPT],
+                                               const bool (&ok)[VPT], const uint4 (&wv)[VPT],
+                                               const uint4 (&pr)[VPT], const uint4 (&ad)[VPT],
+                                               const uint4 (&ad2)[VPT], Src& src) {
   constexpr int S = N + 1;             // sources: bank[0..N-1], new prefix
   constexpr int K = 2 * S;             // per-token sums: (ss_i, d_i)
   constexpr int KP = Pow2<K>::value;
   constexpr int SHIFT = 5 - Pow2<K>::log2;
+  const int lane = t.lane, warp = t.warp;
 
-  __shared__ float red[32][KP];        // per-warp partials of R1
-  __shared__ float xchg[KP];           // CTA totals of R1, read by the cluster
-  __shared__ float red2[32];           // per-warp sum of h^2, read by the cluster
+  // ---- fold (the updated prefix is stored at the end: a global store in
+  // flight would make the release barriers below wait for it)
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) src.set_new_prefix(k, fold_chunk<ADD2>(pr[k], ad[k], ad2[k]));
 
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int nwarps = blockDim.x >> 5;
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t csize = cluster_nctarank();
-  const int c0 = static_cast<int>(crank) * p.cpc;
+  // ---- per-source sums of squares and dot products with w
+  float part[KP];
+#pragma unroll
+  for (int i = 0; i < S; ++i) {
+    float ss = 0.f, d = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const uint4 u = src.get(i, k);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xv = elem(u, e);
+        ss = fma_rn(xv, xv, ss);
+        d = fma_rn(elem(wv[k], e), xv, d);
+      }
+    }
+    part[2 * i] = ss;
+    part[2 * i + 1] = d;
+  }
+#pragma unroll
+  for (int i = K; i < KP; ++i) part[i] = 0.f;
+  src.fence();
+
+  // ---- R1: warp transpose-reduction, CTA sum, push to every CTA, barrier
+  const float wtot = warp_transpose_reduce<KP>(part, lane);
+  if ((lane & ((1 << SHIFT) - 1)) == 0) x.red[warp][lane >> SHIFT] = wtot;
+  __syncthreads();
+  if (warp == 0 && lane < KP) {
+    float s = 0.f;
+    for (int w = 0; w < t.nwarps; ++w) s += x.red[w][lane];
+    const uint32_t a = smem_u32(&x.xin1[t.crank][lane]);
+    for (uint32_t c = 0; c < t.csize; ++c) st_dsmem(dsmem_map(a, c), s);
+  }
+  cluster_sync();
+  float tot = 0.f;
+  if (lane < KP) {
+    for (uint32_t c = 0; c < t.csize; ++c) tot += x.xin1[c][lane];
+  }
+
+  // ---- logits and softmax, lane i < S holds source i
+  const float ss_i = __shfl_sync(FULL, tot, (2 * lane) & 31);
+  const float d_i = __shfl_sync(FULL, tot, (2 * lane + 1) & 31);
+  const float logit = (lane < S) ? rsqrtf(__fmaf_rn(ss_i, p.inv_h, p.eps)) * d_i : -INFINITY;
+  const float mx = warp_max(logit);
+  const float ex = (lane < S) ? __expf(logit - mx) : 0.f;
+  const float den = warp_sum(ex);
+  const float alpha_l = ex / den;
+  float alpha[S];
+#pragma unroll
+  for (int i = 0; i < S; ++i) alpha[i] = __shfl_sync(FULL, alpha_l, i);
+
+  uint4 gv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) gv[k] = ok[k] ? ld_keep(p.gamma + jj[k]) : make_uint4(0, 0, 0, 0);
+
+  // ---- mixture h = sum_i alpha_i v_i, and sum h^2
+  float h[VPT][8];
+  float q = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    {
+      const uint4 u = src.get(0, k);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[k][e] = mul_rn(alpha[0], elem(u, e));
+    }
+#pragma unroll
+    for (int i = 1; i < S; ++i) {
+      const uint4 u = src.get(i, k);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[k][e] = fma_rn(alpha[i], elem(u, e), h[k][e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q = fma_rn(h[k][e], h[k][e], q);
+  }
+
+  // ---- R2: warp sum, lane c pushes it to CTA c, barrier, every warp sums
+  // all warps of all CTAs in one fixed order
+  q = warp_sum(q);
+  if (static_cast<uint32_t>(lane) < t.csize)
+    st_dsmem(dsmem_map(smem_u32(&x.xin2[t.crank * t.nwarps + warp]), lane), q);
+  cluster_sync();
+  const int nw_total = static_cast<int>(t.csize) * t.nwarps;
+  float qq = 0.f;
+  for (int idx = lane; idx < nw_total; idx += 32) qq += x.xin2[idx];
+  qq = warp_sum(qq);
+  const float rh = rsqrtf(__fmaf_rn(qq, p.inv_h, p.eps));
+
+  // ---- outputs
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    if (ok[k]) {
+      st_out(p.new_prefix + row + jj[k], src.new_prefix(k));
+      uint4 o;
+      o.x = pack_bf16x2(mul_rn(mul_rn(h[k][0], rh), elem(gv[k], 0)),
+                        mul_rn(mul_rn(h[k][1], rh), elem(gv[k], 1)));
+      o.y = pack_bf16x2(mul_rn(mul_rn(h[k][2], rh), elem(gv[k], 2)),
+                        mul_rn(mul_rn(h[k][3], rh), elem(gv[k], 3)));
+      o.z = pack_bf16x2(mul_rn(mul_rn(h[k][4], rh), elem(gv[k], 4)),
+                        mul_rn(mul_rn(h[k][5], rh), elem(gv[k], 5)));
+      o.w = pack_bf16x2(mul_rn(mul_rn(h[k][6], rh), elem(gv[k], 6)),
+                        mul_rn(mul_rn(h[k][7], rh), elem(gv[k], 7)));
+      st_out(p.out + row + jj[k], o);
+    }
+  }
+}
+
+__device__ __forceinline__ Thread thread_info() {
+  Thread t;
+  t.lane = threadIdx.x & 31;
+  t.warp = threadIdx.x >> 5;
+  t.nwarps = blockDim.x >> 5;
+  t.crank = cluster_ctarank();
+  t.csize = cluster_nctarank();
+  return t;
+}
+
+// ---------------------------------------------------------------- kernels
+
+// Loads straight to registers; each cluster handles tokens blockIdx.y,
+// blockIdx.y + gridDim.y, ...
+template <int N, bool ADD2, int VPT, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params p) {
+  __shared__ Exchange x;
+  const Thread t = thread_info();
+  const int c0 = static_cast<int>(t.crank) * p.cpc;
   const int cend = min(c0 + p.cpc, p.H8);
-
   int jj[VPT];
   bool ok[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
-    jj[k] = c0 + tid + k * static_cast<int>(blockDim.x);
+    jj[k] = c0 + static_cast<int>(threadIdx.x) + k * static_cast<int>(blockDim.x);
     ok[k] = jj[k] < cend;
   }
 
@@ -261,16 +477,18 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // complete (and its writes to be visible) before touching global memory.
   // Without the launch attribute this returns at once.
   griddep_wait();
+  // Distributed shared memory may be written only once every CTA of the
+  // cluster runs: arrive now, wait just before the first push.
+  cluster_arrive_relaxed();
 
   uint4 wv[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) wv[k] = ok[k] ? ld_keep(p.w + jj[k]) : make_uint4(0, 0, 0, 0);
 
+  bool first = true;
   for (int m = blockIdx.y; m < p.M; m += gridDim.y) {
     const size_t row = static_cast<size_t>(m) * p.H8;
-
-    // ---- load every source chunk once
-    uint4 v[S][VPT];
+    uint4 v[N + 1][VPT];
     uint4 pr[VPT], ad[VPT], ad2[VPT];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -282,130 +500,106 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
       for (int i = 0; i < N; ++i)
         v[i][k] = ok[k] ? ld_stream(p.bank + i * p.bank_stride + row + jj[k]) : z;
     }
-
     // Let the next kernel on the stream be scheduled once every CTA of this
     // grid is past its loads; it still waits for this grid to finish.
     griddep_launch_dependents();
-
-    // ---- fold (the updated prefix is stored at the end: a global store in
-    // flight would make every release barrier below wait for it)
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) v[N][k] = fold_chunk<ADD2>(pr[k], ad[k], ad2[k]);
-
-    // ---- per-source sums of squares and dot products with w
-    float part[KP];
-#pragma unroll
-    for (int i = 0; i < S; ++i) {
-      float ss = 0.f, d = 0.f;
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float x = elem(v[i][k], e);
-          ss = fma_rn(x, x, ss);
-          d = fma_rn(elem(wv[k], e), x, d);
-        }
-      }
-      part[2 * i] = ss;
-      part[2 * i + 1] = d;
+    if (first) {
+      cluster_wait();
+      first = false;
     }
-#pragma unroll
-    for (int i = K; i < KP; ++i) part[i] = 0.f;
-    // Keep only the packed BF16 words alive across the reductions: without
-    // this the compiler reuses the unpacked floats of the pass above in the
-    // mixture and holds twice the registers.
-#pragma unroll
-    for (int i = 0; i < S; ++i)
-#pragma unroll
-      for (int k = 0; k < VPT; ++k)
-        asm volatile("" : "+r"(v[i][k].x), "+r"(v[i][k].y), "+r"(v[i][k].z), "+r"(v[i][k].w));
-
-    // ---- R1: warp, CTA, cluster
-    const float wtot = warp_transpose_reduce<KP>(part, lane);
-    if ((lane & ((1 << SHIFT) - 1)) == 0) red[warp][lane >> SHIFT] = wtot;
-    __syncthreads();
-    if (warp == 0 && lane < KP) {
-      float s = 0.f;
-      for (int w = 0; w < nwarps; ++w) s += red[w][lane];
-      xchg[lane] = s;
-    }
-    cluster_sync();
-    float tot = 0.f;
-    if (lane < KP) {
-      for (uint32_t c = 0; c < csize; ++c) tot += ld_dsmem(dsmem_addr(&xchg[lane], c));
-    }
-
-    // ---- logits and softmax, lane i < S holds source i
-    const float ss_i = __shfl_sync(FULL, tot, (2 * lane) & 31);
-    const float d_i = __shfl_sync(FULL, tot, (2 * lane + 1) & 31);
-    const float logit = (lane < S) ? rsqrtf(__fmaf_rn(ss_i, p.inv_h, p.eps)) * d_i : -INFINITY;
-    const float mx = warp_max(logit);
-    const float ex = (lane < S) ? __expf(logit - mx) : 0.f;
-    const float den = warp_sum(ex);
-    const float alpha_l = ex / den;
-    float alpha[S];
-#pragma unroll
-    for (int i = 0; i < S; ++i) alpha[i] = __shfl_sync(FULL, alpha_l, i);
-
-    uint4 gv[VPT];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) gv[k] = ok[k] ? ld_keep(p.gamma + jj[k]) : make_uint4(0, 0, 0, 0);
-
-    // ---- mixture h = sum_i alpha_i v_i, and sum h^2
-    float h[VPT][8];
-    float q = 0.f;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float acc = mul_rn(alpha[0], elem(v[0][k], e));
-#pragma unroll
-        for (int i = 1; i < S; ++i) acc = fma_rn(alpha[i], elem(v[i][k], e), acc);
-        h[k][e] = acc;
-        q = fma_rn(acc, acc, q);
-      }
-    }
-
-    // ---- R2: warp, then every warp reads all warps of all CTAs
-    q = warp_sum(q);
-    if (lane == 0) red2[warp] = q;
-    cluster_sync();
-    const int nw_total = static_cast<int>(csize) * nwarps;
-    float qq = 0.f;
-    for (int idx = lane; idx < nw_total; idx += 32)
-      qq += ld_dsmem(dsmem_addr(&red2[idx % nwarps], static_cast<uint32_t>(idx / nwarps)));
-    qq = warp_sum(qq);
-    // This CTA has consumed every remote value it reads for this token; the
-    // arrive orders nothing else, so it can be relaxed.
-    cluster_arrive_relaxed();
-    const float rh = rsqrtf(__fmaf_rn(qq, p.inv_h, p.eps));
-
-    // ---- outputs
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      if (ok[k]) {
-        st_out(p.new_prefix + row + jj[k], v[N][k]);
-        uint4 o;
-        o.x = pack_bf16x2(mul_rn(mul_rn(h[k][0], rh), elem(gv[k], 0)),
-                          mul_rn(mul_rn(h[k][1], rh), elem(gv[k], 1)));
-        o.y = pack_bf16x2(mul_rn(mul_rn(h[k][2], rh), elem(gv[k], 2)),
-                          mul_rn(mul_rn(h[k][3], rh), elem(gv[k], 3)));
-        o.z = pack_bf16x2(mul_rn(mul_rn(h[k][4], rh), elem(gv[k], 4)),
-                          mul_rn(mul_rn(h[k][5], rh), elem(gv[k], 5)));
-        o.w = pack_bf16x2(mul_rn(mul_rn(h[k][6], rh), elem(gv[k], 6)),
-                          mul_rn(mul_rn(h[k][7], rh), elem(gv[k], 7)));
-        st_out(p.out + row + jj[k], o);
-      }
-    }
-    // No CTA may leave, or overwrite its exchange slots for the next token,
-    // while another CTA of the cluster may still read them.
-    cluster_wait();
+    RegSources<N, VPT> src{v};
+    token_epilogue<N, ADD2, VPT>(p, x, t, row, jj, ok, wv, pr, ad, ad2, src);
   }
+  if (first) cluster_wait();  // a cluster with no token still pairs its arrive
 }
 
-// Host-side launcher of one instantiation (defined in attnres_launch.cuh).
+// Persistent streaming kernel: each cluster walks tokens blockIdx.y +
+// k * gridDim.y; every thread copies its own chunk of each source row of the
+// token STAGES-1 steps ahead into its private slots of a shared-memory ring
+// (cp.async), so HBM reads stay in flight through the reductions of the
+// current token.  The bank chunks are read from the ring once per pass (sums,
+// then mixture) instead of being held in registers, which keeps the kernel
+// small enough for several CTAs per SM.  A thread only ever reads slots it
+// filled itself, so the ring needs no barrier beyond cp.async.wait_group.
+template <int N, bool ADD2, int MAXT, int MINB, int STAGES>
+__global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p) {
+  constexpr int ROWS = N + (ADD2 ? 3 : 2);   // prefix, add, [add2], bank[0..N-1]
+  extern __shared__ uint4 ring[];             // [STAGES][ROWS][blockDim.x]
+  __shared__ Exchange x;
+  const Thread t = thread_info();
+  const int c0 = static_cast<int>(t.crank) * p.cpc;
+  const int cend = min(c0 + p.cpc, p.H8);
+  const int jj1 = c0 + static_cast<int>(threadIdx.x);
+  const int jj[1] = {jj1};
+  const bool ok[1] = {jj1 < cend};
+  const uint32_t ring0 = smem_u32(ring) + threadIdx.x * 16u;
+  const uint32_t row_step = blockDim.x * 16u;
+  const uint32_t stage_step = ROWS * row_step;
+
+  griddep_wait();
+  cluster_arrive_relaxed();
+  const uint4 wv[1] = {ok[0] ? ld_keep(p.w + jj1) : make_uint4(0, 0, 0, 0)};
+
+  auto issue = [&](int m, int stage) {
+    if (m < p.M && ok[0]) {
+      const size_t off = static_cast<size_t>(m) * p.H8 + jj1;
+      uint32_t d = ring0 + stage * stage_step;
+      cp_async16(d, p.prefix + off);
+      d += row_step;
+      cp_async16(d, p.add + off);
+      d += row_step;
+      if (ADD2) {
+        cp_async16(d, p.add2 + off);
+        d += row_step;
+      }
+#pragma unroll
+      for (int i = 0; i < N; ++i, d += row_step) cp_async16(d, p.bank + i * p.bank_stride + off);
+    }
+    cp_async_commit();  // an empty group keeps the group count uniform
+  };
+
+  const int G = gridDim.y;
+  const int m0 = blockIdx.y;
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) issue(m0 + s * G, s);
+  griddep_launch_dependents();
+
+  bool first = true;
+  int stage = 0;
+  for (int m = m0; m < p.M; m += G) {
+    const int ahead = (stage + STAGES - 1) % STAGES;
+    issue(m + (STAGES - 1) * G, ahead);
+    cp_async_wait<STAGES - 1>();
+    uint4 pr[1], ad[1], ad2[1];
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    uint32_t a = ring0 + stage * stage_step;
+    pr[0] = ok[0] ? lds16(a) : z;
+    a += row_step;
+    ad[0] = ok[0] ? lds16(a) : z;
+    a += row_step;
+    ad2[0] = z;
+    if (ADD2) {
+      ad2[0] = ok[0] ? lds16(a) : z;
+      a += row_step;
+    }
+    if (first) {
+      cluster_wait();
+      first = false;
+    }
+    SmemSources<N> src{a, row_step, ok[0], z};
+    token_epilogue<N, ADD2, 1>(p, x, t, static_cast<size_t>(m) * p.H8, jj, ok, wv, pr, ad, ad2, src);
+    stage = (stage + 1 == STAGES) ? 0 : stage + 1;
+  }
+  cp_async_wait<0>();
+  if (first) cluster_wait();
+}
+
+// Host-side launchers of one instantiation (defined in attnres_launch.cuh).
 template <int N, bool ADD2, int VPT, int MAXT, int MINB>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
                          cudaStream_t s);
+template <int N, bool ADD2, int STAGES>
+cudaError_t launch_pipe(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
+                        cudaStream_t s);
 
 }  // namespace attnres

@@ -53,12 +53,93 @@ cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, b
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// The persistent pipelined kernel: up to 256 threads, STAGES tokens in the
+// shared-memory ring (STAGES - 1 in flight while one is reduced).
+constexpr int kPipeMaxT = 256, kPipeMinB = 1;
+
+inline int pipe_rows(int N, bool add2) { return N + (add2 ? 3 : 2); }
+
+inline size_t pipe_smem_bytes(int N, bool add2, int threads, int stages) {
+  return static_cast<size_t>(stages) * pipe_rows(N, add2) * threads * 16u;
+}
+
+// Launch the pipelined kernel with a grid of grid.y clusters; grid.y == 0
+// asks for as many clusters as can be resident at once (capped at M).
+template <int N, bool ADD2, int STAGES>
+cudaError_t launch_pipe(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
+                        cudaStream_t s) {
+  auto kern = attnres_pipe_kernel<N, ADD2, kPipeMaxT, kPipeMinB, STAGES>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const size_t smem = pipe_smem_bytes(N, ADD2, threads, STAGES);
+  // Raise the dynamic shared-memory limit (and opt in to large clusters)
+  // once per device; the limit only grows.
+  static std::atomic<int> smem_set[kMaxDevices];
+  static std::atomic<unsigned char> opted[kMaxDevices];
+  if (static_cast<int>(smem) > smem_set[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    smem_set[dev].store(static_cast<int>(smem), std::memory_order_release);
+  }
+  if (cluster > 8 && !opted[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    opted[dev].store(1, std::memory_order_release);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  if (grid.y == 0) {
+    // Resident clusters for this (threads, cluster, shared memory), cached
+    // per device for the last configuration asked.
+    static std::atomic<long long> cache[kMaxDevices];
+    const long long key = (static_cast<long long>(threads) << 8 | cluster) << 20 | static_cast<long long>(smem >> 4);
+    long long c = cache[dev].load(std::memory_order_acquire);
+    int clusters = 0;
+    if (c != 0 && (c >> 16) == key) {
+      clusters = static_cast<int>(c & 0xffff);
+    } else {
+      cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
+      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (clusters < 1) return cudaErrorInvalidConfiguration;
+      if (clusters > 0xffff) clusters = 0xffff;
+      cache[dev].store(key << 16 | clusters, std::memory_order_release);
+    }
+    grid.y = static_cast<unsigned>(clusters < p.M ? clusters : p.M);
+  }
+  if (grid.y > 65535u) grid.y = 65535u;
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster), grid.y, 1);
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+#define ATTNRES_INSTANTIATE_PIPE(N, ADD2)                                                    \
+  template cudaError_t launch_pipe<N, ADD2, 2>(const Params&, dim3, int, int, bool,          \
+                                               cudaStream_t);                                \
+  template cudaError_t launch_pipe<N, ADD2, 3>(const Params&, dim3, int, int, bool,          \
+                                               cudaStream_t);                                \
+  template cudaError_t launch_pipe<N, ADD2, 4>(const Params&, dim3, int, int, bool,          \
+                                               cudaStream_t);
+
 #define ATTNRES_INSTANTIATE(N, ADD2)                                                       \
   template cudaError_t launch_fused<N, ADD2, kSplitVPT, kSplitMaxT, kSplitMinB>(             \
       const Params&, dim3, int, int, bool, cudaStream_t);                                    \
   template cudaError_t launch_fused<N, ADD2, kStreamVPT, kStreamMaxT, kStreamMinB>(          \
       const Params&, dim3, int, int, bool, cudaStream_t);                                    \
   template cudaError_t launch_fused<N, ADD2, kCtaVPT, kCtaMaxT, kCtaMinB>(                   \
-      const Params&, dim3, int, int, bool, cudaStream_t);
+      const Params&, dim3, int, int, bool, cudaStream_t);                                    \
+  ATTNRES_INSTANTIATE_PIPE(N, ADD2)
 
 }  // namespace attnres

@@ -65,9 +65,10 @@ def _ceil(a, b):
 
 def split_configs(H):
     """Every cluster size whose CTAs fit the split shape (<= 256 threads of 8
-    columns) or the streaming shape (<= 224 threads) for this H, the
-    one-CTA-per-token variant where it fits (<= 448 threads of 16 columns),
-    and the automatic choice (None)."""
+    columns), the register-capped shape (<= 224 threads) or the pipelined
+    persistent kernel (<= 256 threads) for this H, the one-CTA-per-token
+    variant where it fits (<= 448 threads of 16 columns), and the automatic
+    choice (None)."""
     H8 = H // 8
     cfgs = [None]
     for c in range(1, 17):
@@ -76,6 +77,9 @@ def split_configs(H):
     for c in range(1, 17):
         if _ceil(_ceil(H8, c), 32) * 32 <= 224:
             cfgs.append(binding.make_config("stream", cluster=c))
+    for c in range(1, 17):
+        if _ceil(_ceil(H8, c), 32) * 32 <= 256:
+            cfgs.append(binding.make_config("pipe", cluster=c))
     if _ceil(_ceil(H8, 2), 32) * 32 <= 448:
         cfgs.append(binding.make_config("cta"))
     return cfgs
@@ -87,4 +91,6 @@ def cfg_name(c):
     d = c.as_dict()
     if d["variant"] == 1:
         return "cta"
-    return f"{'cluster' if d['variant'] == 2 else 'stream'}{d['cluster']}"
+    name = {2: "cluster", 3: "stream", 4: "pipe"}[d["variant"]]
+    extra = f"s{d['stages']}" if d["stages"] else ""
+    return f"{name}{d['cluster']}{extra}"

@@ -93,5 +93,6 @@ def test_alias_rules():
 
 def test_config_struct_layout():
     c = binding.make_config("cluster", cluster=8, threads=128)
-    assert ctypes.sizeof(c) == 20
-    assert c.as_dict() == {"variant": 2, "cluster": 8, "threads": 128, "grid_tokens": 0, "pdl": 0}
+    assert ctypes.sizeof(c) == 24
+    assert c.as_dict() == {"variant": 2, "cluster": 8, "threads": 128, "grid_tokens": 0, "pdl": 0,
+                           "stages": 0}

@@ -58,6 +58,7 @@ def test_decode_every_variant(cfg, M, N):
 @pytest.mark.parametrize("special_prefix", [False, True])
 @pytest.mark.parametrize("cfg", [None, binding.make_config("cluster", cluster=4),
                                  binding.make_config("stream", cluster=4),
+                                 binding.make_config("pipe", cluster=4),
                                  binding.make_config("cta")], ids=cfg_name)
 def test_bit_exact_stress(special_prefix, cfg):
     inp = wl.stress_inputs(special_prefix=special_prefix)
@@ -230,7 +231,7 @@ def test_ragged_and_small_hidden_sizes(Hs):
 def test_token_loop(grid_tokens):
     """Fewer token CTAs than tokens: each cluster loops over tokens."""
     inp = wl.make_inputs(67, 6, H, seed=11)
-    for variant, cl in (("cluster", 4), ("cluster", 8), ("stream", 4)):
+    for variant, cl in (("cluster", 4), ("cluster", 8), ("stream", 4), ("pipe", 4), ("pipe", 7)):
         cfg = binding.make_config(variant, cluster=cl, grid_tokens=grid_tokens)
         gnp, gout = run_gpu(inp, cfg)
         assert_parity(inp, gnp, gout)
@@ -274,7 +275,7 @@ def test_side_stream_and_plan():
     assert_parity(inp, gnp, gout)
     for M in (1, 8, 16, 32, 8192):
         plan = binding.attnres_plan(M, 12, H)
-        assert plan["variant"] in (1, 2, 3) and plan["threads"] % 32 == 0
+        assert plan["variant"] in (1, 2, 3, 4) and plan["threads"] % 32 == 0
 
 
 def test_invalid_config_rejected_on_device():
@@ -351,3 +352,30 @@ def test_back_to_back_dependent_calls_with_pdl():
                            u16(inp.gamma), inp.eps)
         assert (u16(newp) == ref_np).all()
         Pc = ref_np
+
+
+@pytest.mark.parametrize("stages", [2, 3, 4])
+@pytest.mark.parametrize("cl", [4, 8])
+@pytest.mark.parametrize("add2", [True, False])
+def test_pipe_stages(stages, cl, add2):
+    """The pipelined kernel at every ring depth, with the ring wrapping many
+    times (few resident clusters, many tokens) and a ragged token count."""
+    inp = wl.make_inputs(203, 12, H, seed=70 + stages + cl, add2=add2)
+    cfg = binding.make_config("pipe", cluster=cl, stages=stages, grid_tokens=5)
+    gnp, gout = run_gpu(inp, cfg)
+    assert_parity(inp, gnp, gout, label=f"pipe{cl}s{stages}")
+    auto = binding.make_config("pipe", cluster=cl, stages=stages)
+    gnp2, gout2 = run_gpu(inp, auto)
+    assert (gnp2 == gnp).all() and (gout2 == gout).all()
+
+
+def test_pipe_invalid_stages_rejected():
+    d = wl.make_inputs(4, 12, H, seed=1).to("cuda")
+    out = torch.empty_like(d.prefix)
+    newp = torch.empty_like(d.prefix)
+    for cfg in (binding.make_config("pipe", stages=5), binding.make_config("pipe", stages=1),
+                binding.make_config("cluster", cluster=8, stages=2)):
+        with pytest.raises(binding.AttnResError) as e:
+            binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps,
+                                        out, newp, config=cfg)
+        assert e.value.status == -8
