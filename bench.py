@@ -255,14 +255,15 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU legs
 
-def time_bandwidth(binding, inp, steps, warmup, stream):
-    """K back-to-back calls, each bracketed by CUDA events on `stream`.
-    Returns (total seconds, per-launch seconds list)."""
+def time_bandwidth(binding, inp, steps, warmup, stream, config=None):
+    """Set up K back-to-back calls, each to be bracketed by CUDA events on
+    `stream`; runs the warm-up calls."""
     import torch
     out = torch.empty_like(inp.prefix)
     newp = torch.empty_like(inp.prefix)
     call = lambda: binding.attnres_add_rmsnorm(inp.prefix, inp.add, inp.add2, inp.bank, inp.w,  # noqa: E731
-                                               inp.gamma, inp.eps, out, newp, stream=stream, check=False)
+                                               inp.gamma, inp.eps, out, newp, stream=stream, check=False,
+                                               config=config)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             call()
@@ -405,7 +406,10 @@ def run_ours(args):
     M = args.tokens
     inp = wl.bandwidth_inputs(device="cuda", seed=rank_seed(rank), M=M)
     stream = torch.cuda.Stream()
-    call, ev, t0, t1, out, newp = time_bandwidth(binding, inp, args.steps, args.warmup, stream)
+    config = None
+    if args.variant != "auto" or args.cluster or args.stages:
+        config = binding.make_config(args.variant, cluster=args.cluster, stages=args.stages)
+    call, ev, t0, t1, out, newp = time_bandwidth(binding, inp, args.steps, args.warmup, stream, config)
     nbytes = algorithmic_bytes(M, N_BW, H)
 
     # soak: the same calls back to back so that the clock samples see steady load
@@ -482,7 +486,7 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1) BF16 tensors)",
         "config": {"workload": WORKLOAD if M == M_BW else WORKLOAD.replace("M=8192", f"M={M}"), "M": M, "N": N_BW, "H": H, "add2": True,
                    "bytes_per_call": nbytes, "l2": "inputs (2.0 GB) larger than L2, no flush",
-                   "plan": binding.attnres_plan(M, N_BW, H),
+                   "plan": binding.attnres_plan(M, N_BW, H) if config is None else config.as_dict(),
                    "parallelism": f"dp{ws} (each rank its own 8192 tokens)"},
         "us_per_call": round(total_s / args.steps * 1e6, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -516,6 +520,10 @@ def main(argv=None):
                     help="back-to-back calls before the timed region, under the clock sampler")
     ap.add_argument("--tokens", type=int, default=M_BW,
                     help="tokens of the bandwidth workload (smaller only for profiling runs)")
+    ap.add_argument("--variant", default="auto", choices=("auto", "cta", "cluster", "stream", "pipe"),
+                    help="pin the launch variant of the bandwidth workload (profiling)")
+    ap.add_argument("--cluster", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

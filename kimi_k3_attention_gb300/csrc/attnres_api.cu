@@ -97,11 +97,12 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
   };
   if (c->variant == 0) {
     // Latency regime (M <= 64): spread each token over enough CTAs that
-    // M * cluster covers the SMs.  Streaming regime: the smallest cluster
-    // whose CTAs fit the occupancy-capped shape, so that several tokens are
-    // in flight on every SM.
-    if (M > 64 && min_cluster(kPipeMaxT) <= 16) {
-      c->variant = 4;
+    // M * cluster covers the SMs.  Streaming regime: the register-capped
+    // shape with CTAs of at most 128 threads (a cluster of 7 for H = 7168),
+    // so that many tokens are in flight on every SM.
+    if (M > 64 && min_cluster(128) <= 16) {
+      c->variant = 3;
+      if (c->cluster == 0) c->cluster = min_cluster(128);
     } else {
       c->variant = 2;
       if (c->cluster == 0) {
