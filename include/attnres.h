@@ -163,6 +163,22 @@ const char* attnres_status_string(int status);
  * library (0 if none). */
 int attnres_last_cuda_error(void);
 
+/* Status word the kernels of the current device write, for failures they
+ * cannot return: bit 0 (ATTNRES_DEVICE_WAIT_TIMEOUT) is set when a CTA of a
+ * cluster waited longer than the limit for its peers' partial sums (the
+ * call's outputs are then wrong).  Reads it into *bits (and zeroes it when
+ * `clear` is non-zero).  Synchronous: waits for the device's work to finish.
+ * No correct call sets a bit. */
+#define ATTNRES_DEVICE_WAIT_TIMEOUT 1u
+int attnres_device_status(unsigned int* bits, int clear);
+
+/* Test hook for the failure path.  From the next launch on, every exchange
+ * of partial sums expects `extra_bytes` (0..4096) more than its peers send,
+ * so its waits expire after `wait_ns` (0 = the default of 200 ms, at most
+ * 10 s); the kernel then sets ATTNRES_DEVICE_WAIT_TIMEOUT and finishes
+ * without hanging.  (0, 0) restores normal operation.  Process-wide. */
+int attnres_debug_exchange(int extra_bytes, long long wait_ns);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int attnres_version(void);
 

@@ -19,6 +19,7 @@ STATUS = {
     -4: "ATTNRES_ERR_ALIAS", -5: "ATTNRES_ERR_EPS", -6: "ATTNRES_ERR_CUDA",
     -7: "ATTNRES_ERR_DEVICE", -8: "ATTNRES_ERR_CONFIG",
 }
+ATTNRES_DEVICE_WAIT_TIMEOUT = 1
 VARIANTS = {"auto": 0, "cta": 1, "cluster": 2, "stream": 3, "pipe": 4}
 
 # Every symbol include/attnres.h declares.
@@ -28,6 +29,8 @@ EXPORTS = (
     "attnres_plan",
     "attnres_status_string",
     "attnres_last_cuda_error",
+    "attnres_device_status",
+    "attnres_debug_exchange",
     "attnres_version",
 )
 
@@ -73,6 +76,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attnres_last_cuda_error.restype = i
     lib.attnres_version.argtypes = []
     lib.attnres_version.restype = i
+    lib.attnres_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
+    lib.attnres_device_status.restype = i
+    lib.attnres_debug_exchange.argtypes = [i, ctypes.c_longlong]
+    lib.attnres_debug_exchange.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -169,3 +176,15 @@ def attnres_plan(M, N, H, has_add2=True) -> dict:
 
 def version() -> int:
     return load().attnres_version()
+
+
+def device_status(clear=False) -> int:
+    """The kernels' status bits on the current device (0 = no failure)."""
+    v = ctypes.c_uint(0)
+    _check(load().attnres_device_status(ctypes.byref(v), int(bool(clear))))
+    return v.value
+
+
+def debug_exchange(extra_bytes=0, wait_ns=0):
+    """Test hook: make every exchange wait for bytes that never come."""
+    _check(load().attnres_debug_exchange(int(extra_bytes), int(wait_ns)))

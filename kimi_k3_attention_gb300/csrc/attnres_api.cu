@@ -13,11 +13,22 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 
+// Status word written by the kernels (bit 0: an exchange wait timed out),
+// one per device that loads the library.
+__device__ unsigned int g_device_status;
+
 struct DeviceInfo {
   std::atomic<int> state{0};  // 0 unknown, 1 ok, 2 wrong architecture
   std::atomic<int> sms{0};
+  std::atomic<unsigned int*> status{nullptr};
 };
 DeviceInfo g_dev[kMaxDevices];
+
+// Exchange-wait limit and the test hook that makes every exchange expect
+// bytes that never come (see attnres_debug_exchange).
+constexpr long long kDefaultWaitNs = 200LL * 1000 * 1000;
+std::atomic<long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<unsigned int> g_extra_tx{0};
 
 int fail_cuda(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -40,11 +51,24 @@ int current_device(int* sms) {
       return fail_cuda(e);
     d.sms.store(count, std::memory_order_relaxed);
     st = (major == 10 && minor == 3) ? 1 : 2;
+    if (st == 1) {
+      // The device address of this device's status word, taken with the
+      // device current (the host-side symbol is not a device address).
+      void* ptr = nullptr;
+      if ((e = cudaGetSymbolAddress(&ptr, g_device_status)) != cudaSuccess) return fail_cuda(e);
+      d.status.store(static_cast<unsigned int*>(ptr), std::memory_order_relaxed);
+    }
     d.state.store(st, std::memory_order_release);
   }
   if (st != 1) return ATTNRES_ERR_DEVICE;
   *sms = d.sms.load(std::memory_order_relaxed);
   return ATTNRES_OK;
+}
+
+unsigned int* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return g_dev[dev].status.load(std::memory_order_relaxed);
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -236,6 +260,9 @@ extern "C" int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const
   p.cpc = (p.H8 + c.cluster - 1) / c.cluster;
   p.eps = eps;
   p.inv_h = 1.0f / static_cast<float>(H);
+  p.status = device_status_ptr();
+  p.wait_ns = static_cast<unsigned long long>(g_wait_ns.load(std::memory_order_relaxed));
+  p.extra_tx = g_extra_tx.load(std::memory_order_relaxed);
 
   const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -293,5 +320,28 @@ extern "C" const char* attnres_status_string(int status) {
 }
 
 extern "C" int attnres_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" int attnres_device_status(unsigned int* bits, int clear) {
+  if (!bits) return ATTNRES_ERR_NULL;
+  int sms = 0;
+  int st = current_device(&sms);
+  if (st != ATTNRES_OK) return st;
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_device_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned int));
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  return ATTNRES_OK;
+}
+
+extern "C" int attnres_debug_exchange(int extra_bytes, long long wait_ns) {
+  if (extra_bytes < 0 || extra_bytes > 4096 || wait_ns < 0 || wait_ns > 10LL * 1000 * 1000 * 1000)
+    return ATTNRES_ERR_CONFIG;
+  g_extra_tx.store(static_cast<unsigned int>(extra_bytes), std::memory_order_relaxed);
+  g_wait_ns.store(wait_ns == 0 ? kDefaultWaitNs : wait_ns, std::memory_order_relaxed);
+  return ATTNRES_OK;
+}
 
 extern "C" int attnres_version(void) { return 100; }

@@ -14,19 +14,21 @@
 //           them into flush-to-zero forms (TensorRT-LLM PR #20546, "Op")
 //   stats   ss_i = sum v^2 and d_i = w.v for the N+1 sources, one pass
 //   R1      2(N+1) partial sums: warp transpose-reduction, CTA sum in shared
-//           memory, then every CTA pushes its totals into the shared memory
-//           of every CTA of the cluster (distributed shared memory) and one
-//           cluster barrier publishes them
+//           memory, then every CTA stores its totals into the shared memory
+//           of every CTA of the cluster with st.async, each store counted on
+//           the receiver's mbarrier, which the receiver waits on
 //   softmax every warp evaluates logits and softmax redundantly from the same
 //           totals in the same order, so all warps of all CTAs agree bitwise
 //   mix     h = sum_i alpha_i v_i from registers (no second read)
-//   R2      sum h^2: warp reduction, pushed to every CTA, one cluster barrier
+//   R2      sum h^2: warp reduction, st.async to every CTA, mbarrier wait
 //   out     bf16(h * rsqrt(mean(h^2) + eps) * gamma) and new_prefix stored
 //
-// Every reduction has a fixed order, so results are deterministic.  The
-// kernels have no spin-waits: the only waits are the hardware CTA and
-// cluster barriers, which every thread of every CTA reaches on the same path,
-// and cp.async.wait_group, which completes with the copies it waits for.
+// Every reduction has a fixed order, so results are deterministic.  Waits:
+// the CTA barrier, one cluster barrier at start-up (every thread of every CTA
+// reaches it on the same path), cp.async.wait_group (completes with its
+// copies), and the exchange mbarriers, whose waits are bounded in time: on
+// expiry the kernel sets a bit in the library's status word, stops waiting,
+// and stays resident for the same bound before exiting.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -49,7 +51,13 @@ struct Params {
   int cpc;                // chunks owned by one CTA of the cluster
   float eps;
   float inv_h;            // 1 / H
+  unsigned int* status;   // library status word of this device (bit 0: a wait timed out)
+  unsigned long long wait_ns;  // limit of every exchange wait
+  unsigned int extra_tx;  // test hook: bytes every exchange expects beyond what is sent
 };
+
+// Status bits written by the kernels.
+constexpr unsigned int kStatusWaitTimeout = 1u;
 
 constexpr unsigned FULL = 0xffffffffu;
 
@@ -185,6 +193,60 @@ __device__ __forceinline__ void st_dsmem(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// ---- mbarrier and remote-store primitives of the cluster exchange
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make mbarrier initialisation visible to the other CTAs of the cluster.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Arrive once and expect `tx` bytes of remote stores in the current phase.
+__device__ __forceinline__ void mbar_arm(uint32_t bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of parity `parity` to complete, for at most `limit_ns`.
+static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                               unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Store one float into another CTA's shared memory and count its 4 bytes
+// on that CTA's mbarrier (both addresses are shared::cluster addresses).
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr),
+               "f"(v), "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -261,23 +323,78 @@ struct Pow2 {
 
 // Shared memory of the per-token reductions.
 //   red:  per-warp partials of R1 (local)
-//   xin1: R1 totals pushed by each CTA of the cluster, indexed by its rank
+//   xin1: R1 totals pushed by each CTA of the cluster (st.async), by rank
 //   xin2: per-warp sums of h^2 pushed by each CTA, index rank * warps + warp
-// A CTA writes into a peer's xin1 only after the R2 barrier of the previous
-// token (which the peer passed after reading its xin1), and into xin2 only
-// after the R1 barrier of the same token (which the peer passed after
-// reading its xin2 of the previous token): two barriers per token, none at
-// exit, because no CTA touches another's shared memory after the R2 barrier.
+//   bar1, bar2: mbarriers counting the bytes of xin1 / xin2 of one token
+// Protocol per token k (phase parity k & 1 on both mbarriers):
+//   R1: warp 0 of every CTA stores its KP totals into xin1[rank] of every
+//       CTA with st.async; every thread waits on bar1; thread 0 then re-arms
+//       bar1 for token k+1.
+//   R2: lane c of every warp stores the warp's sum of h^2 into CTA c; every
+//       thread waits on bar2; thread 0 re-arms bar2.
+// A peer's next store into xin1 (token k+1) needs this CTA's R2(k) stores,
+// which follow this CTA's reads of xin1(k) and its re-arm of bar1; its next
+// store into xin2 needs this CTA's R1(k+1) stores, which follow the reads of
+// xin2(k) and the re-arm of bar2.  So slots are never overwritten early, no
+// phase can complete while a local thread still waits on the previous one,
+// and the transaction count never runs ahead of its arming.  No CTA reads
+// another's shared memory, so there is no barrier at exit.
 struct Exchange {
   float red[32][32];
   float xin1[16][32];
   float xin2[512];
+  unsigned long long bar1;
+  unsigned long long bar2;
 };
 
 struct Thread {
   int lane, warp, nwarps;
   uint32_t crank, csize;
+  uint32_t phase;   // parity of the current token's exchange phase
+  bool failed;      // an exchange wait timed out: stop waiting, report it
 };
+
+// Bytes each CTA expects per token: KP totals from every CTA (R1) and one
+// float per warp of every CTA (R2).
+__device__ __forceinline__ uint32_t r1_bytes(int kp, const Thread& t, const Params& p) {
+  return static_cast<uint32_t>(kp) * t.csize * 4u + p.extra_tx;
+}
+__device__ __forceinline__ uint32_t r2_bytes(const Thread& t, const Params& p) {
+  return static_cast<uint32_t>(t.nwarps) * t.csize * 4u + p.extra_tx;
+}
+
+// Once per kernel, before the first exchange: thread 0 initialises and arms
+// both mbarriers; the start of the cluster handshake (arrive now, wait
+// before the first remote store) both publishes them and guarantees every
+// CTA of the cluster runs.
+template <int KP>
+__device__ __forceinline__ void exchange_init(Exchange& x, const Thread& t, const Params& p) {
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&x.bar1), 1);
+    mbar_init(smem_u32(&x.bar2), 1);
+    mbar_arm(smem_u32(&x.bar1), r1_bytes(KP, t, p));
+    mbar_arm(smem_u32(&x.bar2), r2_bytes(t, p));
+    fence_mbar_init();
+  }
+  cluster_arrive_relaxed();
+}
+
+__device__ __forceinline__ void exchange_wait(uint32_t bar, Thread& t, const Params& p) {
+  if (t.failed || mbar_try_wait(bar, t.phase)) return;
+  if (!mbar_wait_bounded(bar, t.phase, p.wait_ns)) {
+    t.failed = true;
+    atomicOr(p.status, kStatusWaitTimeout);
+  }
+}
+
+// After a timed-out wait a peer may still be storing into this CTA's shared
+// memory: stay resident (bounded) before exiting.
+__device__ __forceinline__ void exchange_exit(const Thread& t, const Params& p) {
+  if (!t.failed) return;
+  const unsigned long long t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < p.wait_ns) {
+  }
+}
 
 // Where a token's sources live between the two passes over them.
 //   RegSources:  all N+1 chunks in registers (loaded once from HBM).
@@ -323,7 +440,7 @@ struct SmemSources {
 // wv the pseudo-query chunks; masked chunks (ok false) are zeros and store
 // nothing.
 template <int N, bool ADD2, int VPT, class Src>
-__device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, const Thread& t,
+__device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thread& t,
                                                size_t row, const int (&jj)[VPT],
                                                const bool (&ok)[VPT], const uint4 (&wv)[VPT],
                                                const uint4 (&pr)[VPT], const uint4 (&ad)[VPT],
@@ -361,17 +478,19 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, con
   for (int i = K; i < KP; ++i) part[i] = 0.f;
   src.fence();
 
-  // ---- R1: warp transpose-reduction, CTA sum, push to every CTA, barrier
+  // ---- R1: warp transpose-reduction, CTA sum, st.async to every CTA
   const float wtot = warp_transpose_reduce<KP>(part, lane);
   if ((lane & ((1 << SHIFT) - 1)) == 0) x.red[warp][lane >> SHIFT] = wtot;
   __syncthreads();
+  const uint32_t bar1 = smem_u32(&x.bar1), bar2 = smem_u32(&x.bar2);
   if (warp == 0 && lane < KP) {
     float s = 0.f;
     for (int w = 0; w < t.nwarps; ++w) s += x.red[w][lane];
     const uint32_t a = smem_u32(&x.xin1[t.crank][lane]);
-    for (uint32_t c = 0; c < t.csize; ++c) st_dsmem(dsmem_map(a, c), s);
+    for (uint32_t c = 0; c < t.csize; ++c) st_async_f32(dsmem_map(a, c), s, dsmem_map(bar1, c));
   }
-  cluster_sync();
+  exchange_wait(bar1, t, p);
+  if (threadIdx.x == 0 && !t.failed) mbar_arm(bar1, r1_bytes(KP, t, p));  // next token
   float tot = 0.f;
   if (lane < KP) {
     for (uint32_t c = 0; c < t.csize; ++c) tot += x.xin1[c][lane];
@@ -413,12 +532,15 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, con
     for (int e = 0; e < 8; ++e) q = fma_rn(h[k][e], h[k][e], q);
   }
 
-  // ---- R2: warp sum, lane c pushes it to CTA c, barrier, every warp sums
-  // all warps of all CTAs in one fixed order
+  // ---- R2: warp sum, lane c stores it into CTA c, every warp sums all
+  // warps of all CTAs in one fixed order
   q = warp_sum(q);
   if (static_cast<uint32_t>(lane) < t.csize)
-    st_dsmem(dsmem_map(smem_u32(&x.xin2[t.crank * t.nwarps + warp]), lane), q);
-  cluster_sync();
+    st_async_f32(dsmem_map(smem_u32(&x.xin2[t.crank * t.nwarps + warp]), lane), q,
+                 dsmem_map(bar2, lane));
+  exchange_wait(bar2, t, p);
+  if (threadIdx.x == 0 && !t.failed) mbar_arm(bar2, r2_bytes(t, p));  // next token
+  t.phase ^= 1u;
   const int nw_total = static_cast<int>(t.csize) * t.nwarps;
   float qq = 0.f;
   for (int idx = lane; idx < nw_total; idx += 32) qq += x.xin2[idx];
@@ -444,6 +566,11 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, con
   }
 }
 
+template <int N>
+struct KPOf {
+  static constexpr int value = Pow2<2 * (N + 1)>::value;
+};
+
 __device__ __forceinline__ Thread thread_info() {
   Thread t;
   t.lane = threadIdx.x & 31;
@@ -451,6 +578,8 @@ __device__ __forceinline__ Thread thread_info() {
   t.nwarps = blockDim.x >> 5;
   t.crank = cluster_ctarank();
   t.csize = cluster_nctarank();
+  t.phase = 0;
+  t.failed = false;
   return t;
 }
 
@@ -461,7 +590,7 @@ __device__ __forceinline__ Thread thread_info() {
 template <int N, bool ADD2, int VPT, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params p) {
   __shared__ Exchange x;
-  const Thread t = thread_info();
+  Thread t = thread_info();
   const int c0 = static_cast<int>(t.crank) * p.cpc;
   const int cend = min(c0 + p.cpc, p.H8);
   int jj[VPT];
@@ -478,8 +607,9 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // Without the launch attribute this returns at once.
   griddep_wait();
   // Distributed shared memory may be written only once every CTA of the
-  // cluster runs: arrive now, wait just before the first push.
-  cluster_arrive_relaxed();
+  // cluster runs and has set up its mbarriers: arrive now, wait just before
+  // the first remote store.
+  exchange_init<KPOf<N>::value>(x, t, p);
 
   uint4 wv[VPT];
 #pragma unroll
@@ -511,6 +641,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     token_epilogue<N, ADD2, VPT>(p, x, t, row, jj, ok, wv, pr, ad, ad2, src);
   }
   if (first) cluster_wait();  // a cluster with no token still pairs its arrive
+  exchange_exit(t, p);
 }
 
 // Persistent streaming kernel: each cluster walks tokens blockIdx.y +
@@ -526,7 +657,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
   constexpr int ROWS = N + (ADD2 ? 3 : 2);   // prefix, add, [add2], bank[0..N-1]
   extern __shared__ uint4 ring[];             // [STAGES][ROWS][blockDim.x]
   __shared__ Exchange x;
-  const Thread t = thread_info();
+  Thread t = thread_info();
   const int c0 = static_cast<int>(t.crank) * p.cpc;
   const int cend = min(c0 + p.cpc, p.H8);
   const int jj1 = c0 + static_cast<int>(threadIdx.x);
@@ -537,7 +668,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
   const uint32_t stage_step = ROWS * row_step;
 
   griddep_wait();
-  cluster_arrive_relaxed();
+  exchange_init<KPOf<N>::value>(x, t, p);
   const uint4 wv[1] = {ok[0] ? ld_keep(p.w + jj1) : make_uint4(0, 0, 0, 0)};
 
   auto issue = [&](int m, int stage) {
@@ -592,6 +723,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
   }
   cp_async_wait<0>();
   if (first) cluster_wait();
+  exchange_exit(t, p);
 }
 
 // Host-side launchers of one instantiation (defined in attnres_launch.cuh).

@@ -37,6 +37,7 @@ def run_gpu(inp, config=None, stream=None):
     binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps,
                                 out.t, newp.t, stream=stream, config=config)
     torch.cuda.synchronize()
+    assert binding.device_status() == 0, "a kernel reported a failure"
     assert out.guards_intact(), "write outside out"
     assert newp.guards_intact(), "write outside new_prefix"
     return u16(newp.t), u16(out.t)

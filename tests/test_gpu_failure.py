@@ -1,0 +1,52 @@
+"""The kernels' failure path on the GPU, without a fault: a test hook makes
+every exchange of partial sums wait for bytes that never come; the waits
+must expire, the kernel must finish and report it in the library's status
+word, and normal calls must work again afterwards."""
+import pytest
+import torch
+
+from kimi_k3_attention_gb300 import binding
+from kimi_k3_attention_gb300 import workloads as wl
+
+from gpu_helpers import assert_parity, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+H = wl.H_MODEL
+
+
+@pytest.fixture(autouse=True)
+def _restore():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.device_status(clear=True)
+    yield
+    binding.debug_exchange(0, 0)
+    binding.device_status(clear=True)
+
+
+@pytest.mark.parametrize("cfg", [binding.make_config("cluster", cluster=4),
+                                 binding.make_config("cluster", cluster=16),
+                                 binding.make_config("pipe", cluster=4, grid_tokens=2),
+                                 binding.make_config("cta")],
+                         ids=["cluster4", "cluster16", "pipe4", "cta"])
+def test_exchange_wait_expires_and_reports(cfg):
+    inp = wl.make_inputs(5, 3, H, seed=81).to("cuda")
+    out = torch.empty_like(inp.prefix)
+    newp = torch.empty_like(inp.prefix)
+    binding.debug_exchange(extra_bytes=4, wait_ns=2_000_000)      # 2 ms
+    binding.attnres_add_rmsnorm(inp.prefix, inp.add, inp.add2, inp.bank, inp.w, inp.gamma,
+                                inp.eps, out, newp, config=cfg)
+    torch.cuda.synchronize()                                        # finishes, no hang
+    status = binding.device_status(clear=True)
+    assert status & binding.ATTNRES_DEVICE_WAIT_TIMEOUT
+    binding.debug_exchange(0, 0)
+    gnp, gout = run_gpu(inp.to("cpu"), cfg)                         # normal again
+    assert_parity(inp.to("cpu"), gnp, gout)
+
+
+def test_debug_hook_bounds():
+    with pytest.raises(binding.AttnResError):
+        binding.debug_exchange(extra_bytes=-1)
+    with pytest.raises(binding.AttnResError):
+        binding.debug_exchange(extra_bytes=4, wait_ns=11 * 10 ** 9)
