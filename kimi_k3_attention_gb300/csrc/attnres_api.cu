@@ -112,7 +112,7 @@ int round_up32(int x) { return (x + 31) & ~31; }
 // hold, less the kernel's static exchange buffers and a little slack.
 constexpr size_t kPipeSmemMax = 227 * 1024 - sizeof(Exchange) - 1024;
 
-int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
+int resolve(int M, int N, bool add2, int H, int /*sms*/, attnres_config* c) {
   const int H8 = H / 8;
   auto min_cluster = [&](int maxt) {
     int cl = 1;
@@ -120,19 +120,23 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
     return cl;
   };
   if (c->variant == 0) {
-    // Latency regime (M <= 64): spread each token over enough CTAs that
-    // M * cluster covers the SMs.  Streaming regime: the register-capped
-    // shape with CTAs of at most 128 threads (a cluster of 7 for H = 7168),
-    // so that many tokens are in flight on every SM.
+    // Latency regime (M <= 64): a cluster per token, sized below.
+    // Streaming regime: the register-capped shape with CTAs of at most 128
+    // threads (a cluster of 7 for H = 7168), so that many tokens are in
+    // flight on every SM.
     if (M > 64 && min_cluster(128) <= 16) {
       c->variant = 3;
       if (c->cluster == 0) c->cluster = min_cluster(128);
     } else {
+      // Measured on GB300 (H = 7168): 8 CTAs of 112 columns per token are
+      // fastest up to 16 tokens, 4 CTAs of 224 columns above; larger
+      // clusters pay more for the exchange than they gain in bandwidth.
       c->variant = 2;
       if (c->cluster == 0) {
-        int cl = min_cluster(kSplitMaxT);
-        while (cl < 16 && M * cl < sms) cl *= 2;
-        c->cluster = cl > 16 ? 16 : cl;
+        const int per_cta = (M <= 16) ? 112 : 224;
+        int cl = (H8 + per_cta - 1) / per_cta;
+        const int lo = min_cluster(kSplitMaxT);
+        c->cluster = cl < lo ? lo : (cl > 16 ? 16 : cl);
       }
     }
   }
