@@ -108,55 +108,6 @@ __device__ __forceinline__ float mul_rn(float a, float b) {
   return r;
 }
 
-// ---- packed float32 pairs (Blackwell f32x2 arithmetic), one 64-bit register
-// pair: low half = element 2j, high half = element 2j+1 of a BF16x2 word.
-typedef unsigned long long f32x2;
-
-__device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-
-__device__ __forceinline__ float f2_lo(f32x2 v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return lo;
-}
-
-__device__ __forceinline__ float f2_hi(f32x2 v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return hi;
-}
-
-// The two BF16 lanes of a word as exact float32 values.
-__device__ __forceinline__ f32x2 bf2_unpack(uint32_t u) {
-  f32x2 r;
-  asm("{\n .reg .b32 lo, hi;\n shl.b32 lo, %1, 16;\n and.b32 hi, %1, 0xffff0000;\n"
-      " mov.b64 %0, {lo, hi};\n}"
-      : "=l"(r)
-      : "r"(u));
-  return r;
-}
-
-// a*b + c and a*b on both halves, round to nearest even, no .ftz.
-__device__ __forceinline__ f32x2 fma2_rn(f32x2 a, f32x2 b, f32x2 c) {
-  f32x2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-
-__device__ __forceinline__ f32x2 mul2_rn(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t word(const uint4& v, int wd) {
-  return wd == 0 ? v.x : wd == 1 ? v.y : wd == 2 ? v.z : v.w;
-}
-
 // Two float32 -> packed BF16x2, each rounded to nearest even (no .ftz form
 // exists for this conversion; subnormal results are kept).  `lo` lands in
 // the low 16 bits.
@@ -505,29 +456,23 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
 #pragma unroll
   for (int k = 0; k < VPT; ++k) src.set_new_prefix(k, fold_chunk<ADD2>(pr[k], ad[k], ad2[k]));
 
-  // ---- per-source sums of squares and dot products with w, on element
-  // pairs (even and odd columns summed separately, then added)
-  f32x2 w2[VPT][4];
-#pragma unroll
-  for (int k = 0; k < VPT; ++k)
-#pragma unroll
-    for (int wd = 0; wd < 4; ++wd) w2[k][wd] = bf2_unpack(word(wv[k], wd));
+  // ---- per-source sums of squares and dot products with w
   float part[KP];
 #pragma unroll
   for (int i = 0; i < S; ++i) {
-    f32x2 ss2 = 0ull, d2 = 0ull;   // +0.0f in both halves
+    float ss = 0.f, d = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const uint4 u = src.get(i, k);
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) {
-        const f32x2 x2 = bf2_unpack(word(u, wd));
-        ss2 = fma2_rn(x2, x2, ss2);
-        d2 = fma2_rn(w2[k][wd], x2, d2);
+      for (int e = 0; e < 8; ++e) {
+        const float xv = elem(u, e);
+        ss = fma_rn(xv, xv, ss);
+        d = fma_rn(elem(wv[k], e), xv, d);
       }
     }
-    part[2 * i] = add_rn(f2_lo(ss2), f2_hi(ss2));
-    part[2 * i + 1] = add_rn(f2_lo(d2), f2_hi(d2));
+    part[2 * i] = ss;
+    part[2 * i + 1] = d;
   }
 #pragma unroll
   for (int i = K; i < KP; ++i) part[i] = 0.f;
@@ -567,28 +512,25 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
 #pragma unroll
   for (int k = 0; k < VPT; ++k) gv[k] = ok[k] ? ld_keep(p.gamma + jj[k]) : make_uint4(0, 0, 0, 0);
 
-  // ---- mixture h = sum_i alpha_i v_i on element pairs, and sum h^2
-  f32x2 h[VPT][4];
-  f32x2 q2 = 0ull;
+  // ---- mixture h = sum_i alpha_i v_i, and sum h^2
+  float h[VPT][8];
+  float q = 0.f;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     {
       const uint4 u = src.get(0, k);
-      const f32x2 a2 = f2_pack(alpha[0], alpha[0]);
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) h[k][wd] = mul2_rn(a2, bf2_unpack(word(u, wd)));
+      for (int e = 0; e < 8; ++e) h[k][e] = mul_rn(alpha[0], elem(u, e));
     }
 #pragma unroll
     for (int i = 1; i < S; ++i) {
       const uint4 u = src.get(i, k);
-      const f32x2 a2 = f2_pack(alpha[i], alpha[i]);
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) h[k][wd] = fma2_rn(a2, bf2_unpack(word(u, wd)), h[k][wd]);
+      for (int e = 0; e < 8; ++e) h[k][e] = fma_rn(alpha[i], elem(u, e), h[k][e]);
     }
 #pragma unroll
-    for (int wd = 0; wd < 4; ++wd) q2 = fma2_rn(h[k][wd], h[k][wd], q2);
+    for (int e = 0; e < 8; ++e) q = fma_rn(h[k][e], h[k][e], q);
   }
-  float q = add_rn(f2_lo(q2), f2_hi(q2));
 
   // ---- R2: warp sum, lane c stores it into CTA c, every warp sums all
   // warps of all CTAs in one fixed order
@@ -610,14 +552,16 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
   for (int k = 0; k < VPT; ++k) {
     if (ok[k]) {
       st_out(p.new_prefix + row + jj[k], src.new_prefix(k));
-      const f32x2 rh2 = f2_pack(rh, rh);
-      uint32_t o[4];
-#pragma unroll
-      for (int wd = 0; wd < 4; ++wd) {
-        const f32x2 y = mul2_rn(mul2_rn(h[k][wd], rh2), bf2_unpack(word(gv[k], wd)));
-        o[wd] = pack_bf16x2(f2_lo(y), f2_hi(y));
-      }
-      st_out(p.out + row + jj[k], make_uint4(o[0], o[1], o[2], o[3]));
+      uint4 o;
+      o.x = pack_bf16x2(mul_rn(mul_rn(h[k][0], rh), elem(gv[k], 0)),
+                        mul_rn(mul_rn(h[k][1], rh), elem(gv[k], 1)));
+      o.y = pack_bf16x2(mul_rn(mul_rn(h[k][2], rh), elem(gv[k], 2)),
+                        mul_rn(mul_rn(h[k][3], rh), elem(gv[k], 3)));
+      o.z = pack_bf16x2(mul_rn(mul_rn(h[k][4], rh), elem(gv[k], 4)),
+                        mul_rn(mul_rn(h[k][5], rh), elem(gv[k], 5)));
+      o.w = pack_bf16x2(mul_rn(mul_rn(h[k][6], rh), elem(gv[k], 6)),
+                        mul_rn(mul_rn(h[k][7], rh), elem(gv[k], 7)));
+      st_out(p.out + row + jj[k], o);
     }
   }
 }
