@@ -149,6 +149,63 @@ int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const void* add2
                            int M, int N, int H, attnres_stream_t stream,
                            const attnres_config* cfg);
 
+/*
+ * attnres_add_rmsnorm_tap -- the fused epilogue that also writes the
+ * pre-norm mixture: h_out[M,H] = bf16(h) (one rounding of the float32 h).
+ * Layers whose hidden state is captured (speculative decoding) need that
+ * tensor; with it they can take the fused path instead of adding first
+ * (TensorRT-LLM PR #20546, section "Model": a capture layer declines the
+ * fold because the tap needs the pre-norm mixture).  h_out must be non-NULL,
+ * 16-byte aligned and overlap no other tensor.  Other arguments as above.
+ */
+int attnres_add_rmsnorm_tap(const void* prefix, const void* add, const void* add2,
+                            const void* bank, const void* w, const void* gamma,
+                            float eps, void* out, void* new_prefix, void* h_out,
+                            int M, int N, int H, attnres_stream_t stream);
+
+/*
+ * attnres_rmsnorm -- the attention-residual + RMSNorm alone, without the
+ * fold: the sources are bank[0..N-1, m] and prefix[m] itself; writes only
+ * out.  This is the op the fused epilogue is measured against (section
+ * "Performance": the fused op's cost over the attention-residual alone).
+ */
+int attnres_rmsnorm(const void* prefix, const void* bank, const void* w,
+                    const void* gamma, float eps, void* out, int M, int N, int H,
+                    attnres_stream_t stream);
+
+/*
+ * attnres_tail_add -- the standalone fold in one kernel:
+ * new_prefix = bf16(prefix + bf16(add + add2)) (or bf16(prefix + add) when
+ * add2 is NULL), elementwise over [M,H], both additions float32 round to
+ * nearest even without flushing subnormals.  The single-kernel addition the
+ * fused epilogue replaces (section "Performance").  new_prefix may be
+ * exactly prefix; it may overlap no other input.
+ */
+int attnres_tail_add(const void* prefix, const void* add, const void* add2,
+                     void* new_prefix, int M, int H, attnres_stream_t stream);
+
+/* All arguments of one call, for attnres_launch. */
+typedef struct {
+  const void* prefix;
+  const void* add;        /* fold != 0: required                          */
+  const void* add2;       /* fold != 0: optional second addend             */
+  const void* bank;
+  const void* w;
+  const void* gamma;
+  float eps;
+  void* out;
+  void* new_prefix;       /* fold != 0: required                          */
+  void* h_out;            /* optional BF16 mixture tap                     */
+  int M, N, H;
+  int fold;               /* 1: fused epilogue; 0: attention-residual alone */
+} attnres_args;
+
+/* Any of the calls above (tail_add excepted) with a pinned configuration
+ * (cfg may be NULL).  The attention-residual alone (fold = 0) exists for
+ * variants 2 and 3 only; other variants return ATTNRES_ERR_CONFIG. */
+int attnres_launch(const attnres_args* args, const attnres_config* cfg,
+                   attnres_stream_t stream);
+
 /* The configuration attnres_add_rmsnorm would launch for (M, N, H) with
  * (has_add2 != 0) or without a second addend on the current device, written
  * to *plan with every field resolved (grid_tokens 0 for variant 4 means

@@ -9,6 +9,10 @@ from .binding import (  # noqa: F401
     Config,
     attnres_add_rmsnorm,
     attnres_add_rmsnorm_raw,
+    attnres_add_rmsnorm_tap,
     attnres_plan,
+    attnres_rmsnorm,
+    attnres_tail_add,
+    launch,
     make_config,
 )

@@ -26,6 +26,10 @@ VARIANTS = {"auto": 0, "cta": 1, "cluster": 2, "stream": 3, "pipe": 4}
 EXPORTS = (
     "attnres_add_rmsnorm",
     "attnres_add_rmsnorm_ex",
+    "attnres_add_rmsnorm_tap",
+    "attnres_rmsnorm",
+    "attnres_tail_add",
+    "attnres_launch",
     "attnres_plan",
     "attnres_status_string",
     "attnres_last_cuda_error",
@@ -48,6 +52,14 @@ class Config(ctypes.Structure):
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class Args(ctypes.Structure):
+    _fields_ = [("prefix", ctypes.c_void_p), ("add", ctypes.c_void_p), ("add2", ctypes.c_void_p),
+                ("bank", ctypes.c_void_p), ("w", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
+                ("eps", ctypes.c_float), ("out", ctypes.c_void_p), ("new_prefix", ctypes.c_void_p),
+                ("h_out", ctypes.c_void_p), ("M", ctypes.c_int), ("N", ctypes.c_int),
+                ("H", ctypes.c_int), ("fold", ctypes.c_int)]
 
 
 _lib = None
@@ -76,6 +88,14 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attnres_last_cuda_error.restype = i
     lib.attnres_version.argtypes = []
     lib.attnres_version.restype = i
+    lib.attnres_add_rmsnorm_tap.argtypes = [vp, vp, vp, vp, vp, vp, f, vp, vp, vp, i, i, i, vp]
+    lib.attnres_add_rmsnorm_tap.restype = i
+    lib.attnres_rmsnorm.argtypes = [vp, vp, vp, vp, f, vp, i, i, i, vp]
+    lib.attnres_rmsnorm.restype = i
+    lib.attnres_tail_add.argtypes = [vp, vp, vp, vp, i, i, vp]
+    lib.attnres_tail_add.restype = i
+    lib.attnres_launch.argtypes = [ctypes.POINTER(Args), ctypes.POINTER(Config), vp]
+    lib.attnres_launch.restype = i
     lib.attnres_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
     lib.attnres_device_status.restype = i
     lib.attnres_debug_exchange.argtypes = [i, ctypes.c_longlong]
@@ -154,6 +174,53 @@ def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, out, new_prefix,
                                         _ptr(gamma), float(eps), _ptr(out), _ptr(new_prefix),
                                         M, N, H, s, ctypes.byref(config))
     _check(st)
+
+
+def attnres_add_rmsnorm_tap(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, h_out,
+                            stream=None):
+    """The fused epilogue that also writes h_out = bf16(h), the pre-norm mixture."""
+    N, M, H = bank.shape
+    _check_tensor("h_out", h_out, (M, H))
+    _check(load().attnres_add_rmsnorm_tap(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(bank),
+                                          _ptr(w), _ptr(gamma), float(eps), _ptr(out),
+                                          _ptr(new_prefix), _ptr(h_out), M, N, H,
+                                          _stream_handle(stream)))
+
+
+def attnres_rmsnorm(prefix, bank, w, gamma, eps, out, stream=None, config: Optional[Config] = None):
+    """The attention-residual + RMSNorm alone: sources bank[0..N-1] and prefix."""
+    N, M, H = bank.shape
+    for name, t, shp in (("prefix", prefix, (M, H)), ("bank", bank, (N, M, H)), ("w", w, (H,)),
+                         ("gamma", gamma, (H,)), ("out", out, (M, H))):
+        _check_tensor(name, t, shp)
+    if config is None:
+        _check(load().attnres_rmsnorm(_ptr(prefix), _ptr(bank), _ptr(w), _ptr(gamma), float(eps),
+                                      _ptr(out), M, N, H, _stream_handle(stream)))
+    else:
+        launch(prefix, None, None, bank, w, gamma, eps, out, None, M=M, N=N, H=H, fold=False,
+               config=config, stream=stream)
+
+
+def attnres_tail_add(prefix, add, add2, new_prefix, stream=None):
+    """The standalone fold: new_prefix = bf16(prefix + bf16(add + add2))."""
+    M, H = prefix.shape
+    for name, t in (("prefix", prefix), ("add", add), ("new_prefix", new_prefix)):
+        _check_tensor(name, t, (M, H))
+    if add2 is not None:
+        _check_tensor("add2", add2, (M, H))
+    _check(load().attnres_tail_add(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(new_prefix), M, H,
+                                   _stream_handle(stream)))
+
+
+def launch(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, h_out=None, M=None, N=None,
+           H=None, fold=True, config: Optional[Config] = None, stream=None):
+    """attnres_launch: any fused call with an optional pinned configuration."""
+    if M is None:
+        N, M, H = bank.shape
+    a = Args(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(bank), _ptr(w), _ptr(gamma), float(eps),
+             _ptr(out), _ptr(new_prefix), _ptr(h_out), int(M), int(N), int(H), int(bool(fold)))
+    _check(load().attnres_launch(ctypes.byref(a), None if config is None else ctypes.byref(config),
+                                 _stream_handle(stream)))
 
 
 def attnres_add_rmsnorm_raw(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, M, N, H,

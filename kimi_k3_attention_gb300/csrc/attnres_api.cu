@@ -79,27 +79,57 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-int validate(const void* prefix, const void* add, const void* add2, const void* bank,
-             const void* w, const void* gamma, float eps, const void* out,
-             const void* new_prefix, int M, int N, int H) {
-  if (!prefix || !add || !bank || !w || !gamma || !out || !new_prefix) return ATTNRES_ERR_NULL;
+// One call of the op, whichever entry point it came through.
+struct Args {
+  const void* prefix;
+  const void* add;
+  const void* add2;
+  const void* bank;
+  const void* w;
+  const void* gamma;
+  float eps;
+  void* out;
+  void* new_prefix;
+  void* h_out;
+  int M, N, H;
+  bool fold;
+};
+
+int validate_shape(int M, int N, int H) {
   if (M < 1 || N < 1 || N > ATTNRES_MAX_N || H < 8 || H > ATTNRES_MAX_H || (H % 8) != 0)
     return ATTNRES_ERR_SHAPE;
-  if (!(eps > 0.f) || !isfinite(eps)) return ATTNRES_ERR_EPS;
-  if (misaligned(prefix) || misaligned(add) || (add2 && misaligned(add2)) || misaligned(bank) ||
-      misaligned(w) || misaligned(gamma) || misaligned(out) || misaligned(new_prefix))
+  return ATTNRES_OK;
+}
+
+int validate(const Args& a) {
+  if (!a.prefix || !a.bank || !a.w || !a.gamma || !a.out) return ATTNRES_ERR_NULL;
+  if (a.fold && (!a.add || !a.new_prefix)) return ATTNRES_ERR_NULL;
+  int st = validate_shape(a.M, a.N, a.H);
+  if (st != ATTNRES_OK) return st;
+  if (!(a.eps > 0.f) || !isfinite(a.eps)) return ATTNRES_ERR_EPS;
+  const void* add = a.fold ? a.add : nullptr;
+  const void* add2 = a.fold ? a.add2 : nullptr;
+  const void* np = a.fold ? a.new_prefix : nullptr;
+  if (misaligned(a.prefix) || (add && misaligned(add)) || (add2 && misaligned(add2)) ||
+      misaligned(a.bank) || misaligned(a.w) || misaligned(a.gamma) || misaligned(a.out) ||
+      (np && misaligned(np)) || (a.h_out && misaligned(a.h_out)))
     return ATTNRES_ERR_ALIGN;
-  const size_t R = static_cast<size_t>(M) * static_cast<size_t>(H) * 2u;
-  const size_t B = R * static_cast<size_t>(N);
-  const size_t V = static_cast<size_t>(H) * 2u;
-  const void* ins[6] = {prefix, add, add2, bank, w, gamma};
-  const size_t insz[6] = {R, R, add2 ? R : 0, B, V, V};
-  for (int i = 0; i < 6; ++i)
-    if (overlaps(out, R, ins[i], insz[i])) return ATTNRES_ERR_ALIAS;
-  if (overlaps(out, R, new_prefix, R)) return ATTNRES_ERR_ALIAS;
-  for (int i = 0; i < 6; ++i) {
-    if (i == 0 && new_prefix == prefix) continue;  // in-place carry-on
-    if (overlaps(new_prefix, R, ins[i], insz[i])) return ATTNRES_ERR_ALIAS;
+  const size_t R = static_cast<size_t>(a.M) * static_cast<size_t>(a.H) * 2u;
+  const size_t B = R * static_cast<size_t>(a.N);
+  const size_t V = static_cast<size_t>(a.H) * 2u;
+  const void* ins[6] = {a.prefix, add, add2, a.bank, a.w, a.gamma};
+  const size_t insz[6] = {R, add ? R : 0, add2 ? R : 0, B, V, V};
+  // out and h_out overlap nothing; new_prefix overlaps no input except being
+  // exactly prefix (in-place carry-on)
+  const void* outs[3] = {a.out, a.h_out, np};
+  for (int o = 0; o < 3; ++o) {
+    if (!outs[o]) continue;
+    for (int i = 0; i < 6; ++i) {
+      if (o == 2 && i == 0 && np == a.prefix) continue;
+      if (overlaps(outs[o], R, ins[i], insz[i])) return ATTNRES_ERR_ALIAS;
+    }
+    for (int q = o + 1; q < 3; ++q)
+      if (outs[q] && overlaps(outs[o], R, outs[q], R)) return ATTNRES_ERR_ALIAS;
   }
   return ATTNRES_OK;
 }
@@ -191,10 +221,26 @@ int resolve(int M, int N, bool add2, int H, int /*sms*/, attnres_config* c) {
 template <int VPT, int MAXT, int MINB>
 cudaError_t dispatch(int N, bool add2, const Params& p, dim3 g, int t, int c, bool pdl,
                      cudaStream_t s) {
-#define ATTNRES_CASE(n)                                                          \
-  case n:                                                                        \
-    return add2 ? launch_fused<n, true, VPT, MAXT, MINB>(p, g, t, c, pdl, s)     \
-                : launch_fused<n, false, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
+#define ATTNRES_CASE(n)                                                                  \
+  case n:                                                                                \
+    return add2 ? launch_fused<n, kFoldAdd2, VPT, MAXT, MINB>(p, g, t, c, pdl, s)        \
+                : launch_fused<n, kFoldAdd, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
+  switch (N) {
+    ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
+    ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
+    ATTNRES_CASE(9) ATTNRES_CASE(10) ATTNRES_CASE(11) ATTNRES_CASE(12)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef ATTNRES_CASE
+}
+
+template <int VPT, int MAXT, int MINB>
+cudaError_t dispatch_nofold(int N, const Params& p, dim3 g, int t, int c, bool pdl,
+                            cudaStream_t s) {
+#define ATTNRES_CASE(n) \
+  case n:               \
+    return launch_fused<n, kNoFold, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
   switch (N) {
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
     ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
@@ -232,6 +278,80 @@ cudaError_t dispatch_pipe(int N, bool add2, int stages, const Params& p, dim3 g,
 #undef ATTNRES_CASE
 }
 
+int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
+  int st = validate(a);
+  if (st != ATTNRES_OK) return st;
+  int sms = 0;
+  if ((st = current_device(&sms)) != ATTNRES_OK) return st;
+  const bool has_add2 = a.fold && a.add2 != nullptr;
+  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0, 0};
+  if ((st = resolve(a.M, a.N, has_add2, a.H, sms, &c)) != ATTNRES_OK) return st;
+  // the attention-residual alone exists in the two fused shapes only
+  if (!a.fold && c.variant != 2 && c.variant != 3) return ATTNRES_ERR_CONFIG;
+
+  Params p;
+  p.prefix = static_cast<const uint4*>(a.prefix);
+  p.add = static_cast<const uint4*>(a.fold ? a.add : nullptr);
+  p.add2 = static_cast<const uint4*>(has_add2 ? a.add2 : nullptr);
+  p.bank = static_cast<const uint4*>(a.bank);
+  p.w = static_cast<const uint4*>(a.w);
+  p.gamma = static_cast<const uint4*>(a.gamma);
+  p.out = static_cast<uint4*>(a.out);
+  p.new_prefix = static_cast<uint4*>(a.fold ? a.new_prefix : nullptr);
+  p.h_out = static_cast<uint4*>(a.h_out);
+  p.M = a.M;
+  p.H8 = a.H / 8;
+  p.bank_stride = static_cast<long long>(a.M) * p.H8;
+  p.cpc = (p.H8 + c.cluster - 1) / c.cluster;
+  p.eps = a.eps;
+  p.inv_h = 1.0f / static_cast<float>(a.H);
+  p.status = device_status_ptr();
+  p.wait_ns = static_cast<unsigned long long>(g_wait_ns.load(std::memory_order_relaxed));
+  p.extra_tx = g_extra_tx.load(std::memory_order_relaxed);
+
+  const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
+  const bool pdl = c.pdl >= 0;
+  cudaError_t e;
+  if (!a.fold && c.variant == 2)
+    e = dispatch_nofold<kSplitVPT, kSplitMaxT, kSplitMinB>(a.N, p, grid, c.threads, c.cluster, pdl, s);
+  else if (!a.fold)
+    e = dispatch_nofold<kStreamVPT, kStreamMaxT, kStreamMinB>(a.N, p, grid, c.threads, c.cluster,
+                                                              pdl, s);
+  else if (c.variant == 1)
+    e = dispatch<kCtaVPT, kCtaMaxT, kCtaMinB>(a.N, has_add2, p, grid, c.threads, 1, pdl, s);
+  else if (c.variant == 2)
+    e = dispatch<kSplitVPT, kSplitMaxT, kSplitMinB>(a.N, has_add2, p, grid, c.threads, c.cluster,
+                                                    pdl, s);
+  else if (c.variant == 3)
+    e = dispatch<kStreamVPT, kStreamMaxT, kStreamMinB>(a.N, has_add2, p, grid, c.threads,
+                                                       c.cluster, pdl, s);
+  else
+    e = dispatch_pipe(a.N, has_add2, c.stages, p, grid, c.threads, c.cluster, pdl, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ATTNRES_OK;
+}
+
+Args make_args(const void* prefix, const void* add, const void* add2, const void* bank,
+               const void* w, const void* gamma, float eps, void* out, void* new_prefix,
+               void* h_out, int M, int N, int H, bool fold) {
+  Args a;
+  a.prefix = prefix;
+  a.add = add;
+  a.add2 = add2;
+  a.bank = bank;
+  a.w = w;
+  a.gamma = gamma;
+  a.eps = eps;
+  a.out = out;
+  a.new_prefix = new_prefix;
+  a.h_out = h_out;
+  a.M = M;
+  a.N = N;
+  a.H = H;
+  a.fold = fold;
+  return a;
+}
+
 }  // namespace
 }  // namespace attnres
 
@@ -242,49 +362,9 @@ extern "C" int attnres_add_rmsnorm_ex(const void* prefix, const void* add, const
                                       float eps, void* out, void* new_prefix, int M, int N,
                                       int H, attnres_stream_t stream,
                                       const attnres_config* cfg) {
-  int st = validate(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, M, N, H);
-  if (st != ATTNRES_OK) return st;
-  int sms = 0;
-  if ((st = current_device(&sms)) != ATTNRES_OK) return st;
-  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0, 0};
-  if ((st = resolve(M, N, add2 != nullptr, H, sms, &c)) != ATTNRES_OK) return st;
-
-  Params p;
-  p.prefix = static_cast<const uint4*>(prefix);
-  p.add = static_cast<const uint4*>(add);
-  p.add2 = static_cast<const uint4*>(add2);
-  p.bank = static_cast<const uint4*>(bank);
-  p.w = static_cast<const uint4*>(w);
-  p.gamma = static_cast<const uint4*>(gamma);
-  p.out = static_cast<uint4*>(out);
-  p.new_prefix = static_cast<uint4*>(new_prefix);
-  p.M = M;
-  p.H8 = H / 8;
-  p.bank_stride = static_cast<long long>(M) * p.H8;
-  p.cpc = (p.H8 + c.cluster - 1) / c.cluster;
-  p.eps = eps;
-  p.inv_h = 1.0f / static_cast<float>(H);
-  p.status = device_status_ptr();
-  p.wait_ns = static_cast<unsigned long long>(g_wait_ns.load(std::memory_order_relaxed));
-  p.extra_tx = g_extra_tx.load(std::memory_order_relaxed);
-
-  const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool has_add2 = add2 != nullptr;
-  const bool pdl = c.pdl >= 0;
-  cudaError_t e;
-  if (c.variant == 1)
-    e = dispatch<kCtaVPT, kCtaMaxT, kCtaMinB>(N, has_add2, p, grid, c.threads, 1, pdl, s);
-  else if (c.variant == 2)
-    e = dispatch<kSplitVPT, kSplitMaxT, kSplitMinB>(N, has_add2, p, grid, c.threads, c.cluster,
-                                                    pdl, s);
-  else if (c.variant == 3)
-    e = dispatch<kStreamVPT, kStreamMaxT, kStreamMinB>(N, has_add2, p, grid, c.threads,
-                                                       c.cluster, pdl, s);
-  else
-    e = dispatch_pipe(N, has_add2, c.stages, p, grid, c.threads, c.cluster, pdl, s);
-  if (e != cudaSuccess) return fail_cuda(e);
-  return ATTNRES_OK;
+  return run(make_args(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, nullptr, M, N, H,
+                       true),
+             cfg, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
@@ -293,6 +373,58 @@ extern "C" int attnres_add_rmsnorm(const void* prefix, const void* add, const vo
                                    attnres_stream_t stream) {
   return attnres_add_rmsnorm_ex(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, M, N, H,
                                 stream, nullptr);
+}
+
+extern "C" int attnres_add_rmsnorm_tap(const void* prefix, const void* add, const void* add2,
+                                       const void* bank, const void* w, const void* gamma,
+                                       float eps, void* out, void* new_prefix, void* h_out, int M,
+                                       int N, int H, attnres_stream_t stream) {
+  if (!h_out) return ATTNRES_ERR_NULL;
+  return run(make_args(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, h_out, M, N, H,
+                       true),
+             nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attnres_rmsnorm(const void* prefix, const void* bank, const void* w,
+                               const void* gamma, float eps, void* out, int M, int N, int H,
+                               attnres_stream_t stream) {
+  return run(make_args(prefix, nullptr, nullptr, bank, w, gamma, eps, out, nullptr, nullptr, M, N,
+                       H, false),
+             nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attnres_launch(const attnres_args* args, const attnres_config* cfg,
+                              attnres_stream_t stream) {
+  if (!args) return ATTNRES_ERR_NULL;
+  return run(make_args(args->prefix, args->add, args->add2, args->bank, args->w, args->gamma,
+                       args->eps, args->out, args->new_prefix, args->h_out, args->M, args->N,
+                       args->H, args->fold != 0),
+             cfg, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attnres_tail_add(const void* prefix, const void* add, const void* add2,
+                                void* new_prefix, int M, int H, attnres_stream_t stream) {
+  if (!prefix || !add || !new_prefix) return ATTNRES_ERR_NULL;
+  if (M < 1 || H < 8 || H > ATTNRES_MAX_H || (H % 8) != 0) return ATTNRES_ERR_SHAPE;
+  if (misaligned(prefix) || misaligned(add) || (add2 && misaligned(add2)) || misaligned(new_prefix))
+    return ATTNRES_ERR_ALIGN;
+  const size_t R = static_cast<size_t>(M) * static_cast<size_t>(H) * 2u;
+  if ((new_prefix != prefix && overlaps(new_prefix, R, prefix, R)) || overlaps(new_prefix, R, add, R) ||
+      overlaps(new_prefix, R, add2, add2 ? R : 0))
+    return ATTNRES_ERR_ALIAS;
+  int sms = 0;
+  int st = current_device(&sms);
+  if (st != ATTNRES_OK) return st;
+  const long long chunks = static_cast<long long>(M) * (H / 8);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint4* p4 = static_cast<const uint4*>(prefix);
+  const uint4* a4 = static_cast<const uint4*>(add);
+  const uint4* b4 = static_cast<const uint4*>(add2);
+  uint4* n4 = static_cast<uint4*>(new_prefix);
+  cudaError_t e = add2 ? launch_tail_add<true>(p4, a4, b4, n4, chunks, sms, true, s)
+                       : launch_tail_add<false>(p4, a4, b4, n4, chunks, sms, true, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ATTNRES_OK;
 }
 
 extern "C" int attnres_plan(int M, int N, int H, int has_add2, attnres_config* plan) {

@@ -44,7 +44,8 @@ struct Params {
   const uint4* w;
   const uint4* gamma;
   uint4* out;
-  uint4* new_prefix;
+  uint4* new_prefix;      // unused when the kernel does not fold
+  uint4* h_out;           // optional BF16 copy of the mixture h (NULL: none)
   long long bank_stride;  // chunks between snapshots: M * H8
   int M;
   int H8;                 // 16-byte chunks per row: H / 8
@@ -55,6 +56,13 @@ struct Params {
   unsigned long long wait_ns;  // limit of every exchange wait
   unsigned int extra_tx;  // test hook: bytes every exchange expects beyond what is sent
 };
+
+// What a launch does with the prefix sum.
+//   kFoldAdd:  new_prefix = bf16(prefix + add)            (no second addend)
+//   kFoldAdd2: new_prefix = bf16(prefix + bf16(add + add2))
+//   kNoFold:   the prefix itself is the last source; no addends, no
+//              new_prefix (the attention-residual + RMSNorm alone)
+constexpr int kFoldAdd = 0, kFoldAdd2 = 1, kNoFold = 2;
 
 // Status bits written by the kernels.
 constexpr unsigned int kStatusWaitTimeout = 1u;
@@ -439,7 +447,7 @@ struct SmemSources {
 // addend chunks, src gives the bank chunks (and receives the updated prefix),
 // wv the pseudo-query chunks; masked chunks (ok false) are zeros and store
 // nothing.
-template <int N, bool ADD2, int VPT, class Src>
+template <int N, int MODE, int VPT, class Src>
 __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thread& t,
                                                size_t row, const int (&jj)[VPT],
                                                const bool (&ok)[VPT], const uint4 (&wv)[VPT],
@@ -454,7 +462,8 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
   // ---- fold (the updated prefix is stored at the end: a global store in
   // flight would make the release barriers below wait for it)
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) src.set_new_prefix(k, fold_chunk<ADD2>(pr[k], ad[k], ad2[k]));
+  for (int k = 0; k < VPT; ++k)
+    src.set_new_prefix(k, MODE == kNoFold ? pr[k] : fold_chunk<MODE == kFoldAdd2>(pr[k], ad[k], ad2[k]));
 
   // ---- per-source sums of squares and dot products with w
   float part[KP];
@@ -551,7 +560,15 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     if (ok[k]) {
-      st_out(p.new_prefix + row + jj[k], src.new_prefix(k));
+      if (MODE != kNoFold) st_out(p.new_prefix + row + jj[k], src.new_prefix(k));
+      if (p.h_out != nullptr) {
+        uint4 hv;
+        hv.x = pack_bf16x2(h[k][0], h[k][1]);
+        hv.y = pack_bf16x2(h[k][2], h[k][3]);
+        hv.z = pack_bf16x2(h[k][4], h[k][5]);
+        hv.w = pack_bf16x2(h[k][6], h[k][7]);
+        st_out(p.h_out + row + jj[k], hv);
+      }
       uint4 o;
       o.x = pack_bf16x2(mul_rn(mul_rn(h[k][0], rh), elem(gv[k], 0)),
                         mul_rn(mul_rn(h[k][1], rh), elem(gv[k], 1)));
@@ -587,7 +604,7 @@ __device__ __forceinline__ Thread thread_info() {
 
 // Loads straight to registers; each cluster handles tokens blockIdx.y,
 // blockIdx.y + gridDim.y, ...
-template <int N, bool ADD2, int VPT, int MAXT, int MINB>
+template <int N, int MODE, int VPT, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params p) {
   __shared__ Exchange x;
   Thread t = thread_info();
@@ -624,8 +641,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     for (int k = 0; k < VPT; ++k) {
       const uint4 z = make_uint4(0, 0, 0, 0);
       pr[k] = ok[k] ? ld_stream(p.prefix + row + jj[k]) : z;
-      ad[k] = ok[k] ? ld_stream(p.add + row + jj[k]) : z;
-      ad2[k] = (ADD2 && ok[k]) ? ld_stream(p.add2 + row + jj[k]) : z;
+      ad[k] = (MODE != kNoFold && ok[k]) ? ld_stream(p.add + row + jj[k]) : z;
+      ad2[k] = (MODE == kFoldAdd2 && ok[k]) ? ld_stream(p.add2 + row + jj[k]) : z;
 #pragma unroll
       for (int i = 0; i < N; ++i)
         v[i][k] = ok[k] ? ld_stream(p.bank + i * p.bank_stride + row + jj[k]) : z;
@@ -638,7 +655,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
       first = false;
     }
     RegSources<N, VPT> src{v};
-    token_epilogue<N, ADD2, VPT>(p, x, t, row, jj, ok, wv, pr, ad, ad2, src);
+    token_epilogue<N, MODE, VPT>(p, x, t, row, jj, ok, wv, pr, ad, ad2, src);
   }
   if (first) cluster_wait();  // a cluster with no token still pairs its arrive
   exchange_exit(t, p);
@@ -718,7 +735,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
       first = false;
     }
     SmemSources<N> src{a, row_step, ok[0], z};
-    token_epilogue<N, ADD2, 1>(p, x, t, static_cast<size_t>(m) * p.H8, jj, ok, wv, pr, ad, ad2, src);
+    token_epilogue<N, ADD2 ? kFoldAdd2 : kFoldAdd, 1>(p, x, t, static_cast<size_t>(m) * p.H8, jj,
+                                                     ok, wv, pr, ad, ad2, src);
     stage = (stage + 1 == STAGES) ? 0 : stage + 1;
   }
   cp_async_wait<0>();
@@ -726,12 +744,35 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
   exchange_exit(t, p);
 }
 
+// The standalone fold: new_prefix = bf16(prefix + bf16(add + add2)) (or
+// bf16(prefix + add)) over n 16-byte chunks, grid-stride, 16-byte vectors.
+// The addition that the fused kernel replaces; kept for comparison.
+template <bool ADD2>
+__global__ void __launch_bounds__(256) attnres_tail_add_kernel(const uint4* __restrict__ prefix,
+                                                               const uint4* __restrict__ add,
+                                                               const uint4* __restrict__ add2,
+                                                               uint4* __restrict__ new_prefix,
+                                                               long long n) {
+  griddep_wait();
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride) {
+    const uint4 a2 = ADD2 ? ld_stream(add2 + i) : make_uint4(0, 0, 0, 0);
+    st_out(new_prefix + i, fold_chunk<ADD2>(ld_stream(prefix + i), ld_stream(add + i), a2));
+  }
+  griddep_launch_dependents();
+}
+
 // Host-side launchers of one instantiation (defined in attnres_launch.cuh).
-template <int N, bool ADD2, int VPT, int MAXT, int MINB>
+template <int N, int MODE, int VPT, int MAXT, int MINB>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
                          cudaStream_t s);
 template <int N, bool ADD2, int STAGES>
 cudaError_t launch_pipe(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
                         cudaStream_t s);
+template <bool ADD2>
+cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* add2,
+                            uint4* new_prefix, long long chunks, int sms, bool pdl,
+                            cudaStream_t s);
 
 }  // namespace attnres

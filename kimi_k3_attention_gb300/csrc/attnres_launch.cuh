@@ -19,10 +19,10 @@ constexpr int kSplitVPT = 1, kSplitMaxT = 256, kSplitMinB = 1;
 constexpr int kStreamVPT = 1, kStreamMaxT = 224, kStreamMinB = 3;
 constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 
-template <int N, bool ADD2, int VPT, int MAXT, int MINB>
+template <int N, int MODE, int VPT, int MAXT, int MINB>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
                          cudaStream_t s) {
-  auto kern = attnres_fused_kernel<N, ADD2, VPT, MAXT, MINB>;
+  auto kern = attnres_fused_kernel<N, MODE, VPT, MAXT, MINB>;
   // Cluster sizes above 8 need an opt-in per function and device.
   static std::atomic<unsigned char> opted[kMaxDevices];
   if (cluster > 8) {
@@ -125,6 +125,27 @@ cudaError_t launch_pipe(const Params& p, dim3 grid, int threads, int cluster, bo
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// The standalone fold over M*H/8 chunks: 256-thread CTAs, at most 8 per SM
+// worth of grid (grid-stride beyond that).
+template <bool ADD2>
+cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* add2,
+                            uint4* new_prefix, long long chunks, int sms, bool pdl,
+                            cudaStream_t s) {
+  const long long want = (chunks + 255) / 256;
+  const long long cap = static_cast<long long>(sms) * 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attnres_tail_add_kernel<ADD2>, prefix, add, add2, new_prefix,
+                            chunks);
+}
+
 #define ATTNRES_INSTANTIATE_PIPE(N, ADD2)                                                    \
   template cudaError_t launch_pipe<N, ADD2, 2>(const Params&, dim3, int, int, bool,          \
                                                cudaStream_t);                                \
@@ -134,12 +155,22 @@ cudaError_t launch_pipe(const Params& p, dim3 grid, int threads, int cluster, bo
                                                cudaStream_t);
 
 #define ATTNRES_INSTANTIATE(N, ADD2)                                                       \
-  template cudaError_t launch_fused<N, ADD2, kSplitVPT, kSplitMaxT, kSplitMinB>(             \
-      const Params&, dim3, int, int, bool, cudaStream_t);                                    \
-  template cudaError_t launch_fused<N, ADD2, kStreamVPT, kStreamMaxT, kStreamMinB>(          \
-      const Params&, dim3, int, int, bool, cudaStream_t);                                    \
-  template cudaError_t launch_fused<N, ADD2, kCtaVPT, kCtaMaxT, kCtaMinB>(                   \
-      const Params&, dim3, int, int, bool, cudaStream_t);                                    \
+  template cudaError_t launch_fused<N, ADD2 ? kFoldAdd2 : kFoldAdd, kSplitVPT, kSplitMaxT,     \
+                                    kSplitMinB>(const Params&, dim3, int, int, bool,         \
+                                                cudaStream_t);                               \
+  template cudaError_t launch_fused<N, ADD2 ? kFoldAdd2 : kFoldAdd, kStreamVPT, kStreamMaxT,   \
+                                    kStreamMinB>(const Params&, dim3, int, int, bool,        \
+                                                 cudaStream_t);                              \
+  template cudaError_t launch_fused<N, ADD2 ? kFoldAdd2 : kFoldAdd, kCtaVPT, kCtaMaxT,         \
+                                    kCtaMinB>(const Params&, dim3, int, int, bool,           \
+                                              cudaStream_t);                                 \
   ATTNRES_INSTANTIATE_PIPE(N, ADD2)
+
+// The attention-residual + RMSNorm alone (no fold): split and streaming shapes.
+#define ATTNRES_INSTANTIATE_NOFOLD(N)                                                        \
+  template cudaError_t launch_fused<N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB>(          \
+      const Params&, dim3, int, int, bool, cudaStream_t);                                    \
+  template cudaError_t launch_fused<N, kNoFold, kStreamVPT, kStreamMaxT, kStreamMinB>(       \
+      const Params&, dim3, int, int, bool, cudaStream_t);
 
 }  // namespace attnres

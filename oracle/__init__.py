@@ -7,6 +7,7 @@ imports nothing from the library.
 from .attnres_oracle import (  # noqa: F401
     algorithmic_bytes,
     attnres_add_rmsnorm,
+    attnres_rmsnorm,
     bf16_decode,
     bf16_encode_rne,
     fold,

@@ -48,6 +48,7 @@ __all__ = [
     "fold",
     "mixture",
     "attnres_add_rmsnorm",
+    "attnres_rmsnorm",
     "algorithmic_bytes",
 ]
 
@@ -171,7 +172,8 @@ def mixture(V, w, gamma, eps):
     return {"out": out, "bound": bound, "alpha": alpha, "logits": logits, "h": h}
 
 
-def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, tokens=None, chunk=64):
+def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, tokens=None, chunk=64,
+                        with_h=False):
     """The whole op on BF16 bit patterns.
 
     prefix, add, add2: (M, H) uint16 (add2 may be None);  bank: (N, M, H)
@@ -180,10 +182,12 @@ def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, tokens=None, chu
     tokens: optional index array; when given, only those tokens are computed
     (the fold included), which lets a full-size call be checked on a sample.
 
-    Returns (new_prefix_bits (T, H) uint16, out (T, H) float64, bound (T, H)).
+    Returns (new_prefix_bits (T, H) uint16, out (T, H) float64, bound (T, H)),
+    and with with_h=True also (h (T, H) float64, h_bound (T, H)): the pre-norm
+    mixture and the scale sum_i alpha_i |v_ij| of the terms that meet in it.
     """
     prefix = np.asarray(prefix, dtype=np.uint16)
-    add = np.asarray(add, dtype=np.uint16)
+    add = None if add is None else np.asarray(add, dtype=np.uint16)
     bank = np.asarray(bank, dtype=np.uint16)
     if bank.ndim != 3:
         raise ValueError("bank must be (N, M, H)")
@@ -198,9 +202,14 @@ def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, tokens=None, chu
     np_all = np.empty((len(tokens), H), dtype=np.uint16)
     out_all = np.empty((len(tokens), H), dtype=np.float64)
     bound_all = np.empty((len(tokens), H), dtype=np.float64)
+    h_all = np.empty((len(tokens), H), dtype=np.float64) if with_h else None
+    hb_all = np.empty((len(tokens), H), dtype=np.float64) if with_h else None
     for c0 in range(0, len(tokens), chunk):
         t = tokens[c0:c0 + chunk]
-        np_bits, _ = fold(prefix[t], add[t], None if add2 is None else np.asarray(add2, dtype=np.uint16)[t])
+        if add is None:
+            np_bits = prefix[t]          # no fold: the prefix itself is the source
+        else:
+            np_bits, _ = fold(prefix[t], add[t], None if add2 is None else np.asarray(add2, dtype=np.uint16)[t])
         V = np.empty((len(t), N + 1, H), dtype=np.float64)
         V[:, :N, :] = bf16_decode(bank[:, t, :]).transpose(1, 0, 2)
         V[:, N, :] = bf16_decode(np_bits)
@@ -208,7 +217,23 @@ def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, tokens=None, chu
         np_all[c0:c0 + len(t)] = np_bits
         out_all[c0:c0 + len(t)] = r["out"]
         bound_all[c0:c0 + len(t)] = r["bound"]
+        if with_h:
+            h_all[c0:c0 + len(t)] = r["h"]
+            hb_all[c0:c0 + len(t)] = np.sum(r["alpha"][:, :, None] * np.abs(V), axis=1)
+    if with_h:
+        return np_all, out_all, bound_all, h_all, hb_all
     return np_all, out_all, bound_all
+
+
+def attnres_rmsnorm(prefix, bank, w, gamma, eps, tokens=None, chunk=64, with_h=False):
+    """The attention-residual + RMSNorm alone (no fold): the sources are
+    bank[0..N-1, m] and prefix[m] itself.  TensorRT-LLM PR #20546, section
+    "Performance", measures the fused epilogue against this op.
+
+    Returns (out (T, H) float64, bound (T, H)) [, h, h_bound with with_h]."""
+    r = attnres_add_rmsnorm(prefix, None, None, bank, w, gamma, eps, tokens=tokens, chunk=chunk,
+                            with_h=with_h)
+    return r[1:]
 
 
 def algorithmic_bytes(M, N, H, has_add2):

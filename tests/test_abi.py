@@ -96,3 +96,36 @@ def test_config_struct_layout():
     assert ctypes.sizeof(c) == 24
     assert c.as_dict() == {"variant": 2, "cluster": 8, "threads": 128, "grid_tokens": 0, "pdl": 0,
                            "stages": 0}
+
+
+def test_new_entry_points_validate_on_host():
+    a = _layout()
+    lib = binding.load()
+    vp = ctypes.c_void_p
+    # tap: h_out required, must not overlap out
+    assert lib.attnres_add_rmsnorm_tap(vp(a["prefix"]), vp(a["add"]), vp(a["add2"]), vp(a["bank"]),
+                                       vp(a["w"]), vp(a["gamma"]), 1e-6, vp(a["out"]),
+                                       vp(a["new_prefix"]), None, M, N, H, None) == -1
+    assert lib.attnres_add_rmsnorm_tap(vp(a["prefix"]), vp(a["add"]), vp(a["add2"]), vp(a["bank"]),
+                                       vp(a["w"]), vp(a["gamma"]), 1e-6, vp(a["out"]),
+                                       vp(a["new_prefix"]), vp(a["out"] + 32), M, N, H, None) == -4
+    # alone: no addends needed, but the usual checks hold
+    assert lib.attnres_rmsnorm(vp(a["prefix"]), None, vp(a["w"]), vp(a["gamma"]), 1e-6,
+                               vp(a["out"]), M, N, H, None) == -1
+    assert lib.attnres_rmsnorm(vp(a["prefix"]), vp(a["bank"]), vp(a["w"]), vp(a["gamma"]), 1e-6,
+                               vp(a["bank"] + 64), M, N, H, None) == -4
+    assert lib.attnres_rmsnorm(vp(a["prefix"]), vp(a["bank"]), vp(a["w"]), vp(a["gamma"]), 1e-6,
+                               vp(a["out"]), M, 0, H, None) == -2
+    # tail add
+    assert lib.attnres_tail_add(vp(a["prefix"]), None, None, vp(a["new_prefix"]), M, H, None) == -1
+    assert lib.attnres_tail_add(vp(a["prefix"]), vp(a["add"]), None, vp(a["new_prefix"]), M, 12, None) == -2
+    assert lib.attnres_tail_add(vp(a["prefix"]), vp(a["add"]), None, vp(a["add"] + 16), M, H, None) == -4
+    assert lib.attnres_tail_add(vp(a["prefix"] + 4), vp(a["add"]), None, vp(a["new_prefix"]), M, H, None) == -3
+    # generic launch: NULL args
+    assert lib.attnres_launch(None, None, None) == -1
+
+
+def test_args_struct_layout():
+    # 6 pointers, eps (+4 bytes of padding), 3 pointers, 4 ints: the C layout
+    assert ctypes.sizeof(binding.Args) == 6 * 8 + 8 + 3 * 8 + 4 * 4 == 96
+    assert binding.Args.out.offset == 56 and binding.Args.M.offset == 80

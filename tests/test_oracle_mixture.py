@@ -192,3 +192,33 @@ def test_brute_force_high_precision(H, N, M):
         src = np.concatenate([bank[:, m], bf16_decode(new_p[m])[None]], axis=0)
         ref = _mp_reference(src, w, gamma, 1e-6)
         np.testing.assert_allclose(out[m], ref, rtol=1e-13, atol=1e-15)
+
+
+def test_alone_equals_fold_with_zero_addend():
+    """The attention-residual alone is the fused op with a +0 addend (the
+    fold then leaves every value of the prefix unchanged)."""
+    from oracle import attnres_rmsnorm
+    rng = np.random.default_rng(16)
+    H, N, M = 64, 4, 3
+    bank = _rand_bf16(rng, (N, M, H))
+    prefix = _rand_bf16(rng, (M, H))
+    w = _rand_bf16(rng, (H,), 0.2)
+    gamma = _bf(1 + 0.1 * _rand_bf16(rng, (H,)))
+    out_a, _ = attnres_rmsnorm(_b(prefix), _b(bank), _b(w), _b(gamma), 1e-6)
+    _, out_f, _ = _op(prefix, np.zeros((M, H)), None, bank, w, gamma, 1e-6)
+    np.testing.assert_array_equal(out_a, out_f)
+
+
+@pytest.mark.parametrize("b", [0.5, -1.25])
+def test_closed_form_alone_and_tap(b):
+    """No fold: the prefix (1, -1) is the second source directly; the tap is
+    the pre-norm mixture h = (1, tanh(b r)) of the two-source closed form."""
+    from oracle import attnres_rmsnorm
+    e32 = float(np.float32(1e-6))
+    gamma = [1.5, 0.75]
+    out, _, h, _ = attnres_rmsnorm(_b([[1.0, -1.0]]), _b([[[1.0, 1.0]]]), _b([0.0, b]), _b(gamma),
+                                   1e-6, with_h=True)
+    t = math.tanh(b / math.sqrt(1.0 + e32))
+    s = 1.0 / math.sqrt((1.0 + t * t) / 2.0 + e32)
+    np.testing.assert_allclose(h[0], [1.0, t], rtol=1e-14)
+    np.testing.assert_allclose(out[0], [1.5 * s, 0.75 * t * s], rtol=1e-14)
