@@ -92,9 +92,9 @@ def test_tap_parity(M, N, add2):
 @pytest.mark.parametrize("M,Hs", [(1, 8), (3, 24), (32, 7168), (8192, 7168), (77, 16384)])
 @pytest.mark.parametrize("add2", [True, False])
 def test_tail_add_bit_exact(M, Hs, add2):
-    inp = wl.stress_inputs(M=M if M <= 32 else 32, N=1, H=Hs, seed=M + Hs, special_prefix=True) \
-        if M <= 32 and Hs >= 64 else wl.make_inputs(M, 1, Hs, seed=M + Hs, add2=True)
-    if inp.M != M:
+    if M <= 32 and Hs >= 64:   # subnormal and near-cancelling addends, +-0/subnormal prefix
+        inp = wl.stress_inputs(M=M, N=1, H=Hs, seed=M + Hs, special_prefix=True)
+    else:
         inp = wl.make_inputs(M, 1, Hs, seed=M + Hs, add2=True)
     d = inp.to("cuda")
     newp = Guarded((M, Hs))
