@@ -341,6 +341,115 @@ def decode_latencies(binding, wl, reps=200, replays=5):
     return res
 
 
+def _graph_us(build_calls, s, replays=5):
+    """Capture build_calls() (which enqueues `n` calls on stream s and returns
+    n) in a CUDA graph; median microseconds per call over `replays`."""
+    import torch
+    with torch.cuda.stream(s):
+        build_calls()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        n = build_calls()
+    ts = []
+    for _ in range(replays + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / n)
+    del g
+    return round(statistics.median(ts[1:]), 3)
+
+
+def comparators(binding, reps=200):
+    """The pages' microbenchmark form (TensorRT-LLM PR #20546, "Performance"):
+    the fused op (both addends) against the attention-residual + RMSNorm alone
+    and the standalone single-kernel addition it replaces, in microseconds per
+    call, warm (same buffers) and cold (buffer sets > 2.5x L2)."""
+    import torch
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or (128 << 20)
+    s = torch.cuda.Stream()
+    res = {}
+    for M in (1, 8, 16, 32):
+        for N in (3, 12):
+            per = algorithmic_bytes(M, N, H)
+            nsets = max(2, min(4096, -(-int(2.5 * l2) // per)))
+            g = torch.Generator(device="cuda")
+            g.manual_seed(77 + M + N)
+            rnd = lambda *sh: torch.randn(sh, generator=g, device="cuda").to(torch.bfloat16)  # noqa: E731
+            P, A, A2, B = rnd(nsets, M, H), rnd(nsets, M, H), rnd(nsets, M, H), rnd(nsets, N, M, H)
+            w = (rnd(H).float() / H ** 0.5).to(torch.bfloat16)
+            gam = (1 + 0.1 * rnd(H).float()).to(torch.bfloat16)
+            O, NP = torch.empty_like(P), torch.empty_like(P)
+            ops = {
+                "fused": lambda i: binding.attnres_add_rmsnorm(P[i], A[i], A2[i], B[i], w, gam, 1e-6,
+                                                               O[i], NP[i], stream=s, check=False),
+                "alone": lambda i: binding.attnres_rmsnorm(P[i], B[i], w, gam, 1e-6, O[i], stream=s),
+                "tail_add": lambda i: binding.attnres_tail_add(P[i], A[i], A2[i], NP[i], stream=s),
+            }
+            row = {}
+            for name, op in ops.items():
+                def warm(op=op):
+                    for _ in range(reps):
+                        op(0)
+                    return reps
+
+                def cold(op=op):
+                    n = max(reps, nsets)
+                    for k in range(n):
+                        op(k % nsets)
+                    return n
+                row[name] = {"warm_us": _graph_us(warm, s), "cold_us": _graph_us(cold, s)}
+            row["delta_fused_minus_alone_us"] = {
+                k: round(row["fused"][k] - row["alone"][k], 3) for k in ("warm_us", "cold_us")}
+            res[f"M{M}_N{N}"] = row
+            del P, A, A2, B, O, NP
+    torch.cuda.synchronize()
+    return res
+
+
+def chain_benchmark(binding, wl, layers=25):
+    """The 25-layer decoder chain with deferred MoE tails as one CUDA graph:
+    fused = one call per layer with both addends; eager = the standalone
+    fold kernel, then the attention-residual + RMSNorm alone on the new
+    prefix.  The bank grows 1 -> 12 (a layer that appends writes its new
+    prefix straight into the next bank slot).  Microseconds per layer."""
+    import torch
+    s = torch.cuda.Stream()
+    res = {}
+    for M in (1, 8, 32):
+        emb, p0, L = wl.chain_inputs(M=M, H=H, layers=layers)
+        bank = torch.empty((12, M, H), dtype=torch.bfloat16, device="cuda")
+        bank[0] = emb.to("cuda")
+        P0 = p0.to("cuda")
+        ping = [torch.empty_like(P0), torch.empty_like(P0)]
+        out = torch.empty_like(P0)
+        dev = [(x.w.to("cuda"), x.gamma.to("cuda"), x.routed.to("cuda"), x.shared.to("cuda")) for x in L]
+
+        def chain(fused):
+            P, n = P0, 1
+            for li, (w, g, r, sh) in enumerate(dev):
+                dst = bank[n] if wl.chain_appends_after(li) else ping[li % 2]
+                if fused:
+                    binding.attnres_add_rmsnorm(P, r, sh, bank[:n], w, g, wl.EPS, out, dst,
+                                                stream=s, check=False)
+                else:
+                    binding.attnres_tail_add(P, r, sh, dst, stream=s)
+                    binding.attnres_rmsnorm(dst, bank[:n], w, g, wl.EPS, out, stream=s)
+                P = dst
+                if wl.chain_appends_after(li):
+                    n += 1
+            return layers
+        f = _graph_us(lambda: chain(True), s)
+        e = _graph_us(lambda: chain(False), s)
+        res[f"M{M}"] = {"fused_us_per_layer": f, "eager_us_per_layer": e,
+                        "saving_us_per_layer": round(e - f, 3)}
+    return res
+
+
 def run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_ranks, ws):
     """The same metric through the public API with pinned host buffers: every
     step copies the inputs host->device, calls the op, and copies both
@@ -444,9 +553,13 @@ def run_ours(args):
         e2e = run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_ranks, ws)
 
     decode = None
+    comp = None
+    chain = None
     cpu_base = None
     if rank == 0 and not args.no_decode:
         decode = decode_latencies(binding, wl)
+        comp = comparators(binding)
+        chain = chain_benchmark(binding, wl)
     if rank == 0 and not args.no_cpu_baseline:
         # the oracle on the first tokens of this same workload; the GPU's
         # outputs for those tokens are checked against it on the way
@@ -497,6 +610,8 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "clocks": clocks,
         "decode_us_per_call": decode,
+        "fused_vs_alone_and_tail_add_us": comp,
+        "chain_25_layers": chain,
         "cpu_baseline": cpu_base,
     }
     print(json.dumps(line), flush=True)
