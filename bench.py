@@ -566,7 +566,7 @@ def run_ours(args):
         import numpy as np
         from oracle import check_out
         os.environ.setdefault("OMP_NUM_THREADS", "1")
-        n_sample = 1024
+        n_sample = 4096
         cpu_inp = wl.Inputs(inp.prefix[:n_sample].cpu(), inp.add[:n_sample].cpu(),
                             inp.add2[:n_sample].cpu(), inp.bank[:, :n_sample].cpu().contiguous(),
                             inp.w.cpu(), inp.gamma.cpu(), inp.eps)
