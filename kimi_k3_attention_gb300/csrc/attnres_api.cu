@@ -308,6 +308,7 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   p.status = device_status_ptr();
   p.wait_ns = static_cast<unsigned long long>(g_wait_ns.load(std::memory_order_relaxed));
   p.extra_tx = g_extra_tx.load(std::memory_order_relaxed);
+  p.prefetch = (c.variant == 2 && a.M <= 64) ? 1 : 0;
 
   const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
   const bool pdl = c.pdl >= 0;

@@ -55,6 +55,8 @@ struct Params {
   unsigned int* status;   // library status word of this device (bit 0: a wait timed out)
   unsigned long long wait_ns;  // limit of every exchange wait
   unsigned int extra_tx;  // test hook: bytes every exchange expects beyond what is sent
+  int prefetch;           // 1: warm L2 with the first token's rows before waiting
+                          //    on the previous kernel (latency regime)
 };
 
 // What a launch does with the prefix sum.
@@ -154,6 +156,13 @@ __device__ __forceinline__ uint4 fold_chunk(const uint4& p, const uint4& a, cons
 
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Ask L2 to fetch `bytes` (a multiple of 16) from a 16-byte aligned global
+// address.  A hint only: L2 is coherent, so a prefetch issued before an
+// earlier kernel's writes have landed cannot make a later load stale.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void griddep_launch_dependents() {
@@ -618,9 +627,28 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     ok[k] = jj[k] < cend;
   }
 
+  // Latency regime: let the next kernel on the stream be scheduled at once
+  // (it still waits for this grid to finish before touching memory), and
+  // start pulling this CTA's slice of its first token into L2 while the
+  // previous kernel finishes.
+  if (p.prefetch) {
+    griddep_launch_dependents();
+    const int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3) + 2;
+    if (static_cast<int>(threadIdx.x) < rows && cend > c0 && blockIdx.y < p.M) {
+      const int r = threadIdx.x;
+      const size_t off = static_cast<size_t>(blockIdx.y) * p.H8 + c0;
+      const uint32_t bytes = static_cast<uint32_t>(cend - c0) * 16u;
+      const uint4* src = r < N ? p.bank + r * p.bank_stride + off
+                       : r == N ? p.prefix + off
+                       : r == N + 1 && MODE != kNoFold ? p.add + off
+                       : r == N + 2 && MODE == kFoldAdd2 ? p.add2 + off
+                       : r == rows - 2 ? p.w + c0 : p.gamma + c0;
+      prefetch_l2(src, bytes);
+    }
+  }
   // Programmatic dependent launch: this grid may have been scheduled while
   // the previous kernel on the stream was still running; wait for it to
-  // complete (and its writes to be visible) before touching global memory.
+  // complete (and its writes to be visible) before reading its outputs.
   // Without the launch attribute this returns at once.
   griddep_wait();
   // Distributed shared memory may be written only once every CTA of the
