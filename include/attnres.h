@@ -131,6 +131,12 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *   stages    variant 4 only: tokens held by the shared-memory ring (2..4);
  *             0 = as many as fit 227 KB of shared memory.  Must be 0 for
  *             the other variants.
+ *   prefetch  variants 2 and 3: 1 = before waiting on the previous kernel
+ *             (see pdl), ask L2 to fetch this CTA's rows of its first token;
+ *             2 = let the next kernel be scheduled at once; 3 = both;
+ *             -1 = neither; 0 = the default (1 for variant 2 up to 64
+ *             tokens, else -1).  A prefetch is a hint to a coherent L2 and
+ *             cannot change results.
  */
 typedef struct {
   int variant;
@@ -139,6 +145,7 @@ typedef struct {
   int grid_tokens;
   int pdl;
   int stages;
+  int prefetch;
 } attnres_config;
 
 /* The fused epilogue with a pinned configuration (cfg may be NULL = auto).

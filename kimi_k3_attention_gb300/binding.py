@@ -48,7 +48,7 @@ class AttnResError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("cluster", ctypes.c_int),
                 ("threads", ctypes.c_int), ("grid_tokens", ctypes.c_int), ("pdl", ctypes.c_int),
-                ("stages", ctypes.c_int)]
+                ("stages", ctypes.c_int), ("prefetch", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -129,9 +129,11 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def make_config(variant="auto", cluster=0, threads=0, grid_tokens=0, pdl=0, stages=0) -> Config:
+def make_config(variant="auto", cluster=0, threads=0, grid_tokens=0, pdl=0, stages=0,
+                prefetch=0) -> Config:
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
-    return Config(v, int(cluster), int(threads), int(grid_tokens), int(pdl), int(stages))
+    return Config(v, int(cluster), int(threads), int(grid_tokens), int(pdl), int(stages),
+                  int(prefetch))
 
 
 def _check_tensor(name, t, shape=None):

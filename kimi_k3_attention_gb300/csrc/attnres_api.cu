@@ -215,6 +215,9 @@ int resolve(int M, int N, bool add2, int H, int /*sms*/, attnres_config* c) {
   }
   if (c->pdl < -1 || c->pdl > 1) return ATTNRES_ERR_CONFIG;
   if (c->pdl == 0) c->pdl = 1;
+  if (c->prefetch < -1 || c->prefetch > 3) return ATTNRES_ERR_CONFIG;
+  if (c->prefetch == 0) c->prefetch = (c->variant == 2 && M <= 64) ? 1 : -1;
+  if (c->prefetch > 0 && c->variant != 2 && c->variant != 3) return ATTNRES_ERR_CONFIG;
   return ATTNRES_OK;
 }
 
@@ -284,7 +287,7 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   int sms = 0;
   if ((st = current_device(&sms)) != ATTNRES_OK) return st;
   const bool has_add2 = a.fold && a.add2 != nullptr;
-  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0, 0};
+  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0, 0, 0};
   if ((st = resolve(a.M, a.N, has_add2, a.H, sms, &c)) != ATTNRES_OK) return st;
   // the attention-residual alone exists in the two fused shapes only
   if (!a.fold && c.variant != 2 && c.variant != 3) return ATTNRES_ERR_CONFIG;
@@ -308,7 +311,7 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   p.status = device_status_ptr();
   p.wait_ns = static_cast<unsigned long long>(g_wait_ns.load(std::memory_order_relaxed));
   p.extra_tx = g_extra_tx.load(std::memory_order_relaxed);
-  p.prefetch = (c.variant == 2 && a.M <= 64) ? 1 : 0;
+  p.prefetch = c.prefetch > 0 ? c.prefetch : 0;
 
   const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
   const bool pdl = c.pdl >= 0;
@@ -435,7 +438,7 @@ extern "C" int attnres_plan(int M, int N, int H, int has_add2, attnres_config* p
   int sms = 0;
   int st = current_device(&sms);
   if (st != ATTNRES_OK) return st;
-  attnres_config c = {0, 0, 0, 0, 0, 0};
+  attnres_config c = {0, 0, 0, 0, 0, 0, 0};
   if ((st = resolve(M, N, has_add2 != 0, H, sms, &c)) != ATTNRES_OK) return st;
   *plan = c;
   return ATTNRES_OK;

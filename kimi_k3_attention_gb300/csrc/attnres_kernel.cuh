@@ -55,8 +55,9 @@ struct Params {
   unsigned int* status;   // library status word of this device (bit 0: a wait timed out)
   unsigned long long wait_ns;  // limit of every exchange wait
   unsigned int extra_tx;  // test hook: bytes every exchange expects beyond what is sent
-  int prefetch;           // 1: warm L2 with the first token's rows before waiting
-                          //    on the previous kernel (latency regime)
+  int prefetch;           // bit 0: warm L2 with the first token's rows before
+                          // waiting on the previous kernel; bit 1: also let the
+                          // next kernel be scheduled at once
 };
 
 // What a launch does with the prefix sum.
@@ -631,8 +632,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // (it still waits for this grid to finish before touching memory), and
   // start pulling this CTA's slice of its first token into L2 while the
   // previous kernel finishes.
-  if (p.prefetch) {
-    griddep_launch_dependents();
+  if (p.prefetch & 2) griddep_launch_dependents();
+  if (p.prefetch & 1) {
     const int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3) + 2;
     if (static_cast<int>(threadIdx.x) < rows && cend > c0 && blockIdx.y < p.M) {
       const int r = threadIdx.x;

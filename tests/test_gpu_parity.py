@@ -379,3 +379,28 @@ def test_pipe_invalid_stages_rejected():
             binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps,
                                         out, newp, config=cfg)
         assert e.value.status == -8
+
+
+@pytest.mark.parametrize("prefetch", [-1, 1, 2, 3])
+def test_prefetch_modes_identical(prefetch):
+    """L2 prefetch and early dependent launch change scheduling only; a
+    dependent chain queued without host synchronisation stays exact."""
+    inp = wl.make_inputs(16, 6, H, seed=90)
+    ref = run_gpu(inp, binding.make_config("cluster", cluster=8, prefetch=-1))
+    got = run_gpu(inp, binding.make_config("cluster", cluster=8, prefetch=prefetch))
+    assert (ref[0] == got[0]).all() and (ref[1] == got[1]).all()
+    d = inp.to("cuda")
+    P = d.prefix.clone()
+    outs = []
+    for _ in range(5):
+        out, newp = torch.empty_like(P), torch.empty_like(P)
+        binding.attnres_add_rmsnorm(P, d.add, d.add2, d.bank, d.w, d.gamma, d.eps, out, newp,
+                                    config=binding.make_config("cluster", cluster=8, prefetch=prefetch))
+        outs.append(newp)
+        P = newp
+    torch.cuda.synchronize()
+    from oracle import fold
+    Pc = u16(inp.prefix)
+    for newp in outs:
+        Pc, _ = fold(Pc, u16(inp.add), u16(inp.add2))
+        assert (u16(newp) == Pc).all()
