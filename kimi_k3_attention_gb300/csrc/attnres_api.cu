@@ -96,13 +96,13 @@ struct Args {
 };
 
 int validate_shape(int M, int N, int H) {
-  if (M < 1 || N < 1 || N > ATTNRES_MAX_N || H < 8 || H > ATTNRES_MAX_H || (H % 8) != 0)
+  if (M < 1 || N < 0 || N > ATTNRES_MAX_N || H < 8 || H > ATTNRES_MAX_H || (H % 8) != 0)
     return ATTNRES_ERR_SHAPE;
   return ATTNRES_OK;
 }
 
 int validate(const Args& a) {
-  if (!a.prefix || !a.bank || !a.w || !a.gamma || !a.out) return ATTNRES_ERR_NULL;
+  if (!a.prefix || (a.N > 0 && !a.bank) || !a.w || !a.gamma || !a.out) return ATTNRES_ERR_NULL;
   if (a.fold && (!a.add || !a.new_prefix)) return ATTNRES_ERR_NULL;
   int st = validate_shape(a.M, a.N, a.H);
   if (st != ATTNRES_OK) return st;
@@ -111,13 +111,13 @@ int validate(const Args& a) {
   const void* add2 = a.fold ? a.add2 : nullptr;
   const void* np = a.fold ? a.new_prefix : nullptr;
   if (misaligned(a.prefix) || (add && misaligned(add)) || (add2 && misaligned(add2)) ||
-      misaligned(a.bank) || misaligned(a.w) || misaligned(a.gamma) || misaligned(a.out) ||
+      (a.bank && misaligned(a.bank)) || misaligned(a.w) || misaligned(a.gamma) || misaligned(a.out) ||
       (np && misaligned(np)) || (a.h_out && misaligned(a.h_out)))
     return ATTNRES_ERR_ALIGN;
   const size_t R = static_cast<size_t>(a.M) * static_cast<size_t>(a.H) * 2u;
   const size_t B = R * static_cast<size_t>(a.N);
   const size_t V = static_cast<size_t>(a.H) * 2u;
-  const void* ins[6] = {a.prefix, add, add2, a.bank, a.w, a.gamma};
+  const void* ins[6] = {a.prefix, add, add2, a.N > 0 ? a.bank : nullptr, a.w, a.gamma};
   const size_t insz[6] = {R, add ? R : 0, add2 ? R : 0, B, V, V};
   // out and h_out overlap nothing; new_prefix overlaps no input except being
   // exactly prefix (in-place carry-on)
@@ -229,6 +229,7 @@ cudaError_t dispatch(int N, bool add2, const Params& p, dim3 g, int t, int c, bo
     return add2 ? launch_fused<n, kFoldAdd2, VPT, MAXT, MINB>(p, g, t, c, pdl, s)        \
                 : launch_fused<n, kFoldAdd, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
   switch (N) {
+    ATTNRES_CASE(0)
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
     ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
     ATTNRES_CASE(9) ATTNRES_CASE(10) ATTNRES_CASE(11) ATTNRES_CASE(12)
@@ -245,6 +246,7 @@ cudaError_t dispatch_nofold(int N, const Params& p, dim3 g, int t, int c, bool p
   case n:               \
     return launch_fused<n, kNoFold, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
   switch (N) {
+    ATTNRES_CASE(0)
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
     ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
     ATTNRES_CASE(9) ATTNRES_CASE(10) ATTNRES_CASE(11) ATTNRES_CASE(12)
@@ -272,6 +274,7 @@ cudaError_t dispatch_pipe(int N, bool add2, int stages, const Params& p, dim3 g,
     return add2 ? dispatch_pipe_stages<n, true>(stages, p, g, t, c, pdl, s)          \
                 : dispatch_pipe_stages<n, false>(stages, p, g, t, c, pdl, s);
   switch (N) {
+    ATTNRES_CASE(0)
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
     ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
     ATTNRES_CASE(9) ATTNRES_CASE(10) ATTNRES_CASE(11) ATTNRES_CASE(12)
@@ -433,8 +436,7 @@ extern "C" int attnres_tail_add(const void* prefix, const void* add, const void*
 
 extern "C" int attnres_plan(int M, int N, int H, int has_add2, attnres_config* plan) {
   if (!plan) return ATTNRES_ERR_NULL;
-  if (M < 1 || N < 1 || N > ATTNRES_MAX_N || H < 8 || H > ATTNRES_MAX_H || (H % 8) != 0)
-    return ATTNRES_ERR_SHAPE;
+  if (validate_shape(M, N, H) != ATTNRES_OK) return ATTNRES_ERR_SHAPE;
   int sms = 0;
   int st = current_device(&sms);
   if (st != ATTNRES_OK) return st;
@@ -448,7 +450,7 @@ extern "C" const char* attnres_status_string(int status) {
   switch (status) {
     case ATTNRES_OK: return "ok";
     case ATTNRES_ERR_NULL: return "a required pointer is NULL";
-    case ATTNRES_ERR_SHAPE: return "unsupported shape: need M >= 1, 1 <= N <= 12, 8 <= H <= 16384, H % 8 == 0";
+    case ATTNRES_ERR_SHAPE: return "unsupported shape: need M >= 1, 0 <= N <= 12, 8 <= H <= 16384, H % 8 == 0";
     case ATTNRES_ERR_ALIGN: return "a pointer is not 16-byte aligned";
     case ATTNRES_ERR_ALIAS: return "out overlaps a tensor, or new_prefix overlaps an input other than prefix";
     case ATTNRES_ERR_EPS: return "eps must be finite and > 0";

@@ -1,8 +1,12 @@
 // Explicit instantiations of the attention-residual + RMSNorm alone (no
-// fold), N = 1..12, and of the standalone fold kernel.
+// fold), N = 0..12, of every variant at N = 0 (no snapshots yet: the mixture
+// has the prefix as its only source), and of the standalone fold kernel.
 #include "attnres_launch.cuh"
 
 namespace attnres {
+ATTNRES_INSTANTIATE(0, true)
+ATTNRES_INSTANTIATE(0, false)
+ATTNRES_INSTANTIATE_NOFOLD(0)
 ATTNRES_INSTANTIATE_NOFOLD(1)
 ATTNRES_INSTANTIATE_NOFOLD(2)
 ATTNRES_INSTANTIATE_NOFOLD(3)

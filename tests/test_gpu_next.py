@@ -113,3 +113,35 @@ def test_tail_add_in_place_matches_fused_prefix():
     torch.cuda.synchronize()
     gnp, _ = run_gpu(inp)
     assert (u16(P) == gnp).all()
+
+
+@pytest.mark.parametrize("add2", [True, False])
+def test_no_snapshots(add2):
+    """N = 0 (the first layer): every variant, bank pointer NULL."""
+    from gpu_helpers import split_configs, cfg_name
+    from oracle import attnres_add_rmsnorm as oop
+    for M in (1, 5, 100):
+        inp = wl.make_inputs(M, 1, H, seed=600 + M, add2=add2)
+        d = inp.to("cuda")
+        ref_np, ref_out, bound = oop(u16(inp.prefix), u16(inp.add),
+                                     u16(inp.add2) if add2 else None,
+                                     np.zeros((0, M, H), np.uint16), u16(inp.w), u16(inp.gamma),
+                                     inp.eps)
+        for cfg in split_configs(H):
+            out, newp = Guarded((M, H)), Guarded((M, H))
+            empty = torch.empty((0, M, H), dtype=torch.bfloat16, device="cuda")
+            binding.launch(d.prefix, d.add, d.add2 if add2 else None, empty, d.w, d.gamma, d.eps,
+                           out.t, newp.t, M=M, N=0, H=H, config=cfg)
+            torch.cuda.synchronize()
+            assert binding.device_status() == 0
+            assert out.guards_intact() and newp.guards_intact()
+            assert (u16(newp.t) == ref_np).all(), cfg_name(cfg)
+            assert check_out(u16(out.t), ref_out, bound)["ok"], cfg_name(cfg)
+    # no fold, no snapshots: a plain RMSNorm of the prefix
+    out = torch.empty_like(d.prefix)
+    binding.launch(d.prefix, None, None, None, d.w, d.gamma, d.eps, out, None, M=M, N=0, H=H,
+                   fold=False)
+    torch.cuda.synchronize()
+    ref = torch.nn.functional.rms_norm(inp.prefix.double(), (H,), inp.gamma.double(),
+                                       float(np.float32(inp.eps))).numpy()
+    assert check_out(u16(out), ref, np.abs(ref) + 1e-30)["ok"]

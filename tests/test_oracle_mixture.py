@@ -222,3 +222,17 @@ def test_closed_form_alone_and_tap(b):
     s = 1.0 / math.sqrt((1.0 + t * t) / 2.0 + e32)
     np.testing.assert_allclose(h[0], [1.0, t], rtol=1e-14)
     np.testing.assert_allclose(out[0], [1.5 * s, 0.75 * t * s], rtol=1e-14)
+
+
+def test_no_snapshots_is_rmsnorm_of_the_new_prefix():
+    """N = 0: the updated prefix is the only source, alpha = 1, and out is
+    torch's rms_norm of it."""
+    rng = np.random.default_rng(17)
+    H, M = 96, 4
+    prefix, add, add2 = (_rand_bf16(rng, (M, H)) for _ in range(3))
+    gamma = _bf(1 + 0.1 * _rand_bf16(rng, (H,)))
+    w = _rand_bf16(rng, (H,), 0.3)
+    new_p, out, _ = _op(prefix, add, add2, np.zeros((0, M, H)), w, gamma, 1e-6)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(bf16_decode(new_p)), (H,),
+                                       torch.from_numpy(gamma), float(np.float32(1e-6))).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-15)
