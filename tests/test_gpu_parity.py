@@ -404,3 +404,41 @@ def test_prefetch_modes_identical(prefetch):
     for newp in outs:
         Pc, _ = fold(Pc, u16(inp.add), u16(inp.add2))
         assert (u16(newp) == Pc).all()
+
+
+def _random_cases(n=40, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        H8 = int(rng.choice([1, 3, 8, 40, 100, 257, 896, 897, 1500, 2048]))
+        Hs = 8 * H8
+        M = int(rng.choice([1, 2, 7, 33, 65, 130]))
+        N = int(rng.integers(0, 13))
+        add2 = bool(rng.integers(0, 2))
+        variant = str(rng.choice(["auto", "cta", "cluster", "stream", "pipe"]))
+        lim = {"cta": None, "cluster": 256, "stream": 224, "pipe": 256, "auto": None}[variant]
+        cluster = 0
+        if lim is not None:
+            ok = [c for c in range(1, 17) if -(-(-(-H8 // c)) // 32) * 32 <= lim]
+            if not ok:
+                continue
+            cluster = int(rng.choice(ok))
+        if variant == "cta" and -(-(-(-H8 // 2)) // 32) * 32 > 448:
+            continue
+        gt = int(rng.choice([0, 0, 1, 3]))
+        cases.append((M, N, Hs, add2, variant, cluster, gt, int(rng.integers(0, 10 ** 6))))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=lambda c: "M{}-N{}-H{}-{}-{}{}-g{}".format(
+    c[0], c[1], c[2], "a2" if c[3] else "a1", c[4], c[5], c[6]))
+def test_random_configurations(case):
+    """Seeded random shapes x variants x cluster sizes x grid strides, N = 0
+    included: new_prefix bit-exact, out within tolerance, guards intact."""
+    M, N, Hs, add2, variant, cluster, gt, seed = case
+    inp = wl.make_inputs(M, max(N, 1), Hs, seed=seed, add2=add2)
+    if N == 0:
+        inp.bank = inp.bank[:0]
+    cfg = None if variant == "auto" else binding.make_config(variant, cluster=cluster, grid_tokens=gt)
+    gnp, gout = run_gpu(inp, cfg)
+    assert_parity(inp, gnp, gout, label=str(case))
