@@ -195,9 +195,20 @@ int resolve(int M, int N, bool add2, int H, int /*sms*/, attnres_config* c) {
     if (c->threads < need || c->threads > kPipeMaxT || (c->threads % 32) != 0)
       return ATTNRES_ERR_CONFIG;
     if (c->stages == 0) {
+      // the deepest ring that still lets two CTAs share an SM (228 KB of
+      // shared memory per SM, 1 KB of it reserved per CTA), else the
+      // deepest that fits one
       c->stages = 4;
-      while (c->stages > 2 && pipe_smem_bytes(N, add2, c->threads, c->stages) > kPipeSmemMax)
+      while (c->stages > 2 &&
+             2 * (pipe_smem_bytes(N, add2, c->threads, c->stages) + sizeof(Exchange) + 1024) >
+                 228 * 1024)
         --c->stages;
+      if (2 * (pipe_smem_bytes(N, add2, c->threads, c->stages) + sizeof(Exchange) + 1024) >
+          228 * 1024) {
+        c->stages = 4;
+        while (c->stages > 2 && pipe_smem_bytes(N, add2, c->threads, c->stages) > kPipeSmemMax)
+          --c->stages;
+      }
     }
     if (c->stages < 2 || c->stages > 4 ||
         pipe_smem_bytes(N, add2, c->threads, c->stages) > kPipeSmemMax)

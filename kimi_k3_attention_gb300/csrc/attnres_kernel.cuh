@@ -137,6 +137,19 @@ __device__ __forceinline__ float elem(const uint4& v, int e) {
   return (e & 1) ? bf_hi(u) : bf_lo(u);
 }
 
+// Sums of squares and of products with w for the two BF16 lanes of a word,
+// low lane first: ss += x*x, d += w*x, each a float32 FMA rounded once.  The
+// products of two BF16 values are exact in float32, so the mixed-precision
+// form (BF16 operands, float32 accumulator) gives the same bits as unpacking
+// both operands and using fma.rn.f32, without the unpacking instructions.
+__device__ __forceinline__ void stats_word(uint32_t x, uint32_t w, float& ss, float& d) {
+  asm("{\n .reg .b16 xl, xh, wl, wh;\n mov.b32 {xl, xh}, %2;\n mov.b32 {wl, wh}, %3;\n"
+      " fma.rn.f32.bf16 %0, xl, xl, %0;\n fma.rn.f32.bf16 %1, wl, xl, %1;\n"
+      " fma.rn.f32.bf16 %0, xh, xh, %0;\n fma.rn.f32.bf16 %1, wh, xh, %1;\n}"
+      : "+f"(ss), "+f"(d)
+      : "r"(x), "r"(w));
+}
+
 // One 32-bit word (two BF16 lanes) of the fold.
 template <bool ADD2>
 __device__ __forceinline__ uint32_t fold_word(uint32_t p, uint32_t a, uint32_t a2) {
@@ -300,6 +313,18 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ float half_warp_sum(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float half_warp_max(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
@@ -358,9 +383,9 @@ struct Pow2 {
 // and the transaction count never runs ahead of its arming.  No CTA reads
 // another's shared memory, so there is no barrier at exit.
 struct Exchange {
-  float red[32][32];
-  float xin1[16][32];
-  float xin2[512];
+  float red[16][32];     // up to 16 warps (448-thread CTAs have 14)
+  float xin1[16][32];    // up to 16 CTAs per cluster
+  float xin2[256];       // 16 CTAs x 16 warps
   unsigned long long bar1;
   unsigned long long bar2;
 };
@@ -461,8 +486,9 @@ template <int N, int MODE, int VPT, class Src>
 __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thread& t,
                                                size_t row, const int (&jj)[VPT],
                                                const bool (&ok)[VPT], const uint4 (&wv)[VPT],
+                                               const uint4 (&gv)[VPT],
                                                const uint4 (&pr)[VPT], const uint4 (&ad)[VPT],
-                                               const uint4 (&ad2)[VPT], Src& src) {
+                                               const uint4 (&ad2)[VPT], Src& src, bool& first) {
   constexpr int S = N + 1;             // sources: bank[0..N-1], new prefix
   constexpr int K = 2 * S;             // per-token sums: (ss_i, d_i)
   constexpr int KP = Pow2<K>::value;
@@ -483,12 +509,10 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const uint4 u = src.get(i, k);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float xv = elem(u, e);
-        ss = fma_rn(xv, xv, ss);
-        d = fma_rn(elem(wv[k], e), xv, d);
-      }
+      stats_word(u.x, wv[k].x, ss, d);
+      stats_word(u.y, wv[k].y, ss, d);
+      stats_word(u.z, wv[k].z, ss, d);
+      stats_word(u.w, wv[k].w, ss, d);
     }
     part[2 * i] = ss;
     part[2 * i + 1] = d;
@@ -502,9 +526,17 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
   if ((lane & ((1 << SHIFT) - 1)) == 0) x.red[warp][lane >> SHIFT] = wtot;
   __syncthreads();
   const uint32_t bar1 = smem_u32(&x.bar1), bar2 = smem_u32(&x.bar2);
+  // The first remote store of the kernel waits for every CTA of the cluster
+  // to run and to have set up its mbarriers (see exchange_init).
+  if (first) {
+    cluster_wait();
+    first = false;
+  }
   if (warp == 0 && lane < KP) {
     float s = 0.f;
-    for (int w = 0; w < t.nwarps; ++w) s += x.red[w][lane];
+#pragma unroll
+    for (int w = 0; w < 16; ++w)
+      if (w < t.nwarps) s += x.red[w][lane];
     const uint32_t a = smem_u32(&x.xin1[t.crank][lane]);
     for (uint32_t c = 0; c < t.csize; ++c) st_async_f32(dsmem_map(a, c), s, dsmem_map(bar1, c));
   }
@@ -512,24 +544,23 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
   if (threadIdx.x == 0 && !t.failed) mbar_arm(bar1, r1_bytes(KP, t, p));  // next token
   float tot = 0.f;
   if (lane < KP) {
-    for (uint32_t c = 0; c < t.csize; ++c) tot += x.xin1[c][lane];
+#pragma unroll
+    for (uint32_t c = 0; c < 16; ++c)
+      if (c < t.csize) tot += x.xin1[c][lane];
   }
 
   // ---- logits and softmax, lane i < S holds source i
   const float ss_i = __shfl_sync(FULL, tot, (2 * lane) & 31);
   const float d_i = __shfl_sync(FULL, tot, (2 * lane + 1) & 31);
   const float logit = (lane < S) ? rsqrtf(__fmaf_rn(ss_i, p.inv_h, p.eps)) * d_i : -INFINITY;
-  const float mx = warp_max(logit);
+  // S <= 13 sources sit in lanes 0..15: reduce over 16 lanes
+  const float mx = half_warp_max(logit);
   const float ex = (lane < S) ? __expf(logit - mx) : 0.f;
-  const float den = warp_sum(ex);
+  const float den = half_warp_sum(ex);
   const float alpha_l = ex / den;
   float alpha[S];
 #pragma unroll
   for (int i = 0; i < S; ++i) alpha[i] = __shfl_sync(FULL, alpha_l, i);
-
-  uint4 gv[VPT];
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) gv[k] = ok[k] ? ld_keep(p.gamma + jj[k]) : make_uint4(0, 0, 0, 0);
 
   // ---- mixture h = sum_i alpha_i v_i, and sum h^2
   float h[VPT][8];
@@ -652,14 +683,13 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // complete (and its writes to be visible) before reading its outputs.
   // Without the launch attribute this returns at once.
   griddep_wait();
-  // Distributed shared memory may be written only once every CTA of the
-  // cluster runs and has set up its mbarriers: arrive now, wait just before
-  // the first remote store.
-  exchange_init<KPOf<N>::value>(x, t, p);
 
-  uint4 wv[VPT];
+  uint4 wv[VPT], gv[VPT];
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) wv[k] = ok[k] ? ld_keep(p.w + jj[k]) : make_uint4(0, 0, 0, 0);
+  for (int k = 0; k < VPT; ++k) {
+    wv[k] = ok[k] ? ld_keep(p.w + jj[k]) : make_uint4(0, 0, 0, 0);
+    gv[k] = ok[k] ? ld_keep(p.gamma + jj[k]) : make_uint4(0, 0, 0, 0);
+  }
 
   bool first = true;
   for (int m = blockIdx.y; m < p.M; m += gridDim.y) {
@@ -679,14 +709,14 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // Let the next kernel on the stream be scheduled once every CTA of this
     // grid is past its loads; it still waits for this grid to finish.
     griddep_launch_dependents();
-    if (first) {
-      cluster_wait();
-      first = false;
-    }
+    // Distributed shared memory may be written only once every CTA of the
+    // cluster runs and has set up its mbarriers: set them up and arrive now,
+    // with this token's loads in flight; wait just before the first remote
+    // store.
+    if (first) exchange_init<KPOf<N>::value>(x, t, p);
     RegSources<N, VPT> src{v};
-    token_epilogue<N, MODE, VPT>(p, x, t, row, jj, ok, wv, pr, ad, ad2, src);
+    token_epilogue<N, MODE, VPT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
   }
-  if (first) cluster_wait();  // a cluster with no token still pairs its arrive
   exchange_exit(t, p);
 }
 
@@ -716,6 +746,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
   griddep_wait();
   exchange_init<KPOf<N>::value>(x, t, p);
   const uint4 wv[1] = {ok[0] ? ld_keep(p.w + jj1) : make_uint4(0, 0, 0, 0)};
+  const uint4 gv[1] = {ok[0] ? ld_keep(p.gamma + jj1) : make_uint4(0, 0, 0, 0)};
 
   auto issue = [&](int m, int stage) {
     if (m < p.M && ok[0]) {
@@ -759,17 +790,13 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
       ad2[0] = ok[0] ? lds16(a) : z;
       a += row_step;
     }
-    if (first) {
-      cluster_wait();
-      first = false;
-    }
     SmemSources<N> src{a, row_step, ok[0], z};
     token_epilogue<N, ADD2 ? kFoldAdd2 : kFoldAdd, 1>(p, x, t, static_cast<size_t>(m) * p.H8, jj,
-                                                     ok, wv, pr, ad, ad2, src);
+                                                     ok, wv, gv, pr, ad, ad2, src, first);
     stage = (stage + 1 == STAGES) ? 0 : stage + 1;
   }
   cp_async_wait<0>();
-  if (first) cluster_wait();
+  if (first) cluster_wait();  // a cluster with no token still pairs its arrive
   exchange_exit(t, p);
 }
 
