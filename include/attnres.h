@@ -137,8 +137,7 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *   prefetch  variants 2 and 3: 1 = before waiting on the previous kernel
  *             (see pdl), ask L2 to fetch this CTA's rows of its first token;
  *             2 = let the next kernel be scheduled at once; 3 = both;
- *             -1 = neither; 0 = the default (1 for variant 2 up to 64
- *             tokens, else -1).  A prefetch is a hint to a coherent L2 and
+ *             -1 = neither; 0 = the default (1 up to 96 tokens, else -1).  A prefetch is a hint to a coherent L2 and
  *             cannot change results.
  */
 typedef struct {

@@ -150,24 +150,32 @@ int resolve(int M, int N, bool add2, int H, int /*sms*/, attnres_config* c) {
     return cl;
   };
   if (c->variant == 0) {
-    // Latency regime (M <= 64): a cluster per token, sized below.
-    // Streaming regime: the register-capped shape with CTAs of at most 128
-    // threads (a cluster of 7 for H = 7168), so that many tokens are in
+    // Measured on GB300 at H = 7168 (the cluster sizes below are for that
+    // H and scale with it): up to 32 tokens, a cluster of about 128 / M CTAs
+    // (clamped to 4..8) per token keeps ~128 CTAs per call, one per SM; up
+    // to 48 tokens, 8 CTAs of 112 columns (three fit an SM, still one
+    // wave); then the register-capped shape, 4 CTAs of 224 columns up to 96
+    // tokens and 7 CTAs of 128 columns beyond, where many tokens are in
     // flight on every SM.
-    if (M > 64 && min_cluster(128) <= 16) {
-      c->variant = 3;
-      if (c->cluster == 0) c->cluster = min_cluster(128);
-    } else {
-      // Measured on GB300 (H = 7168): 8 CTAs of 112 columns per token are
-      // fastest up to 16 tokens, 4 CTAs of 224 columns above; larger
-      // clusters pay more for the exchange than they gain in bandwidth.
+    int ref;
+    if (M <= 32) {
       c->variant = 2;
-      if (c->cluster == 0) {
-        const int per_cta = (M <= 16) ? 112 : 224;
-        int cl = (H8 + per_cta - 1) / per_cta;
-        const int lo = min_cluster(kSplitMaxT);
-        c->cluster = cl < lo ? lo : (cl > 16 ? 16 : cl);
-      }
+      ref = (128 + M / 2) / M;
+      ref = ref < 4 ? 4 : (ref > 8 ? 8 : ref);
+    } else if (M <= 48) {
+      c->variant = 2;
+      ref = 8;
+    } else if (M <= 96) {
+      c->variant = 3;
+      ref = 4;
+    } else {
+      c->variant = 3;
+      ref = 7;
+    }
+    if (c->cluster == 0) {
+      const int lo = min_cluster(c->variant == 2 ? kSplitMaxT : kStreamMaxT);
+      int cl = (ref * H8 + 448) / 896;
+      c->cluster = cl < lo ? lo : (cl > 16 ? 16 : cl);
     }
   }
   if (c->variant == 1) {
@@ -227,7 +235,7 @@ int resolve(int M, int N, bool add2, int H, int /*sms*/, attnres_config* c) {
   if (c->pdl < -1 || c->pdl > 1) return ATTNRES_ERR_CONFIG;
   if (c->pdl == 0) c->pdl = 1;
   if (c->prefetch < -1 || c->prefetch > 3) return ATTNRES_ERR_CONFIG;
-  if (c->prefetch == 0) c->prefetch = (c->variant == 2 && M <= 64) ? 1 : -1;
+  if (c->prefetch == 0) c->prefetch = ((c->variant == 2 || c->variant == 3) && M <= 96) ? 1 : -1;
   if (c->prefetch > 0 && c->variant != 2 && c->variant != 3) return ATTNRES_ERR_CONFIG;
   return ATTNRES_OK;
 }
