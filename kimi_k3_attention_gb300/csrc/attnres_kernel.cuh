@@ -678,6 +678,11 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
       prefetch_l2(src, bytes);
     }
   }
+  // Distributed shared memory may be written only once every CTA of the
+  // cluster runs and has set up its mbarriers: set them up and arrive now
+  // (shared memory only, so this overlaps the previous kernel's tail); wait
+  // just before the first remote store.
+  if (blockIdx.y < p.M) exchange_init<KPOf<N>::value>(x, t, p);
   // Programmatic dependent launch: this grid may have been scheduled while
   // the previous kernel on the stream was still running; wait for it to
   // complete (and its writes to be visible) before reading its outputs.
@@ -709,11 +714,6 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // Let the next kernel on the stream be scheduled once every CTA of this
     // grid is past its loads; it still waits for this grid to finish.
     griddep_launch_dependents();
-    // Distributed shared memory may be written only once every CTA of the
-    // cluster runs and has set up its mbarriers: set them up and arrive now,
-    // with this token's loads in flight; wait just before the first remote
-    // store.
-    if (first) exchange_init<KPOf<N>::value>(x, t, p);
     RegSources<N, VPT> src{v};
     token_epilogue<N, MODE, VPT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
   }
@@ -743,8 +743,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
   const uint32_t row_step = blockDim.x * 16u;
   const uint32_t stage_step = ROWS * row_step;
 
-  griddep_wait();
   exchange_init<KPOf<N>::value>(x, t, p);
+  griddep_wait();
   const uint4 wv[1] = {ok[0] ? ld_keep(p.w + jj1) : make_uint4(0, 0, 0, 0)};
   const uint4 gv[1] = {ok[0] ? ld_keep(p.gamma + jj1) : make_uint4(0, 0, 0, 0)};
 
