@@ -595,7 +595,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_s / args.steps * 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, f32 arithmetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
         "data": "synthetic (seeded N(0,1) BF16 tensors)",
         "config": {"workload": WORKLOAD if M == M_BW else WORKLOAD.replace("M=8192", f"M={M}"), "M": M, "N": N_BW, "H": H, "add2": True,
                    "bytes_per_call": nbytes, "l2": "inputs (2.0 GB) larger than L2, no flush",

@@ -442,3 +442,42 @@ def test_random_configurations(case):
     cfg = None if variant == "auto" else binding.make_config(variant, cluster=cluster, grid_tokens=gt)
     gnp, gout = run_gpu(inp, cfg)
     assert_parity(inp, gnp, gout, label=str(case))
+
+
+def test_all_zero_sources():
+    """Every source zero: sums of squares are 0, the norms divide by sqrt(eps),
+    alpha is uniform and out is exactly zero."""
+    inp = wl.make_inputs(4, 5, H, seed=91)
+    for name in ("prefix", "add", "add2"):
+        setattr(inp, name, torch.zeros_like(getattr(inp, name)))
+    inp.bank = torch.zeros_like(inp.bank)
+    gnp, gout = run_gpu(inp)
+    assert_parity(inp, gnp, gout)
+    assert ((gout & 0x7FFF) == 0).all()
+
+
+@pytest.mark.parametrize("scale", [1e15, 1e-30])
+def test_large_and_tiny_magnitudes(scale):
+    """Magnitudes far from 1 while sum(v^2) stays inside float32's range: the
+    RMS normalisations make out scale-free, so it must match the oracle."""
+    inp = wl.make_inputs(8, 6, H, seed=92)
+    for name in ("prefix", "add", "add2"):
+        setattr(inp, name, (getattr(inp, name).float() * scale).to(torch.bfloat16))
+    inp.bank = (inp.bank.float() * scale).to(torch.bfloat16)
+    gnp, gout = run_gpu(inp)
+    assert_parity(inp, gnp, gout)
+
+
+def test_fold_overflow_to_infinity_is_bit_exact():
+    """Sums beyond the largest BF16 round to +-inf in both the fold and the
+    oracle; new_prefix stays bit-exact (outputs of such tokens are not finite
+    and are not compared)."""
+    inp = wl.make_inputs(2, 1, 64, seed=93)
+    big = torch.full((2, 64), 3.0e38).to(torch.bfloat16)
+    inp.prefix, inp.add, inp.add2 = big.clone(), big.clone(), -big.clone() * 0.5
+    inp.add2[:, ::2] = big[:, ::2]
+    gnp, _ = run_gpu(inp)
+    from oracle import fold
+    ref, _ = fold(u16(inp.prefix), u16(inp.add), u16(inp.add2))
+    assert (gnp == ref).all()
+    assert ((ref & 0x7FFF) == 0x7F80).any()
