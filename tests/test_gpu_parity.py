@@ -481,3 +481,64 @@ def test_fold_overflow_to_infinity_is_bit_exact():
     ref, _ = fold(u16(inp.prefix), u16(inp.add), u16(inp.add2))
     assert (gnp == ref).all()
     assert ((ref & 0x7FFF) == 0x7F80).any()
+
+
+def test_two_host_threads_two_streams():
+    """Calls from two host threads on two streams at once (the library's
+    per-device caches are atomics; no device state is shared by calls)."""
+    import threading
+    cases = [wl.make_inputs(32, 12, H, seed=700), wl.make_inputs(300, 5, H, seed=701)]
+    refs = [run_gpu(c) for c in cases]
+    results = [None, None]
+    errors = []
+
+    def worker(i):
+        try:
+            d = cases[i].to("cuda")
+            s = torch.cuda.Stream()
+            outs = []
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    out, newp = torch.empty_like(d.prefix), torch.empty_like(d.prefix)
+                    binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma,
+                                                d.eps, out, newp, stream=s)
+                    outs.append((out, newp))
+            s.synchronize()
+            results[i] = outs
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    th = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert not errors, errors
+    for i in range(2):
+        for out, newp in results[i]:
+            assert (u16(newp) == refs[i][0]).all() and (u16(out) == refs[i][1]).all()
+
+
+def test_cuda_graph_capture_and_replay():
+    """The op captured in a CUDA graph (with programmatic dependent launch
+    between the captured calls) replays to the same bits."""
+    inp = wl.make_inputs(16, 12, H, seed=702)
+    ref_np, ref_out = run_gpu(inp)
+    d = inp.to("cuda")
+    s = torch.cuda.Stream()
+    out, newp = torch.empty_like(d.prefix), torch.empty_like(d.prefix)
+    with torch.cuda.stream(s):
+        binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps, out, newp,
+                                    stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(10):
+            binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps, out,
+                                        newp, stream=s)
+    out.zero_()
+    newp.zero_()
+    with torch.cuda.stream(s):
+        g.replay()
+    torch.cuda.synchronize()
+    assert (u16(newp) == ref_np).all() and (u16(out) == ref_out).all()
