@@ -679,10 +679,13 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     }
   }
   // Distributed shared memory may be written only once every CTA of the
-  // cluster runs and has set up its mbarriers: set them up and arrive now
-  // (shared memory only, so this overlaps the previous kernel's tail); wait
-  // just before the first remote store.
-  if (blockIdx.y < p.M) exchange_init<KPOf<N>::value>(x, t, p);
+  // cluster runs and has set up its mbarriers: set them up and arrive, wait
+  // just before the first remote store.  In the latency regime this happens
+  // here, overlapping the previous kernel's tail (shared memory only); in the
+  // streaming regime after the first token's loads are issued, so that the
+  // set-up does not delay them.
+  const bool early_init = p.prefetch != 0;
+  if (early_init && blockIdx.y < p.M) exchange_init<KPOf<N>::value>(x, t, p);
   // Programmatic dependent launch: this grid may have been scheduled while
   // the previous kernel on the stream was still running; wait for it to
   // complete (and its writes to be visible) before reading its outputs.
@@ -714,6 +717,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // Let the next kernel on the stream be scheduled once every CTA of this
     // grid is past its loads; it still waits for this grid to finish.
     griddep_launch_dependents();
+    if (!early_init && m == static_cast<int>(blockIdx.y)) exchange_init<KPOf<N>::value>(x, t, p);
     RegSources<N, VPT> src{v};
     token_epilogue<N, MODE, VPT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
   }
