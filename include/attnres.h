@@ -134,11 +134,14 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *   stages    variant 4 only: tokens held by the shared-memory ring (2..4);
  *             0 = as many as fit 227 KB of shared memory.  Must be 0 for
  *             the other variants.
- *   prefetch  variants 2 and 3: 1 = before waiting on the previous kernel
- *             (see pdl), ask L2 to fetch this CTA's rows of its first token;
- *             2 = let the next kernel be scheduled at once; 3 = both;
- *             -1 = neither; 0 = the default (1 up to 96 tokens, else -1).  A prefetch is a hint to a coherent L2 and
- *             cannot change results.
+ *   prefetch  variants 2 and 3, a bit mask: 1 = before waiting on the
+ *             previous kernel (see pdl), ask L2 to fetch this CTA's rows of
+ *             its first token; 2 = let the next kernel be scheduled at once;
+ *             4 = while a token is reduced, ask L2 for the CTA's rows of the
+ *             next token it takes (when clusters walk several tokens);
+ *             -1 = none; 0 = the default (1 up to 96 tokens, plus 4 when the
+ *             grid is smaller than M).  A prefetch is a hint to a coherent L2
+ *             and cannot change results.
  */
 typedef struct {
   int variant;

@@ -242,8 +242,12 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
   }
   if (c->pdl < -1 || c->pdl > 1) return ATTNRES_ERR_CONFIG;
   if (c->pdl == 0) c->pdl = 1;
-  if (c->prefetch < -1 || c->prefetch > 3) return ATTNRES_ERR_CONFIG;
-  if (c->prefetch == 0) c->prefetch = ((c->variant == 2 || c->variant == 3) && M <= 96) ? 1 : -1;
+  if (c->prefetch < -1 || c->prefetch > 7) return ATTNRES_ERR_CONFIG;
+  if (c->prefetch == 0) {
+    c->prefetch = ((c->variant == 2 || c->variant == 3) && M <= 96) ? 1 : 0;
+    if (c->variant == 3 && c->grid_tokens < M) c->prefetch |= 4;   // clusters walk tokens
+    if (c->prefetch == 0) c->prefetch = -1;
+  }
   if (c->prefetch > 0 && c->variant != 2 && c->variant != 3) return ATTNRES_ERR_CONFIG;
   return ATTNRES_OK;
 }

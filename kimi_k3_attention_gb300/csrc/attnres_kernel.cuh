@@ -57,7 +57,8 @@ struct Params {
   unsigned int extra_tx;  // test hook: bytes every exchange expects beyond what is sent
   int prefetch;           // bit 0: warm L2 with the first token's rows before
                           // waiting on the previous kernel; bit 1: also let the
-                          // next kernel be scheduled at once
+                          // next kernel be scheduled at once; bit 2: while a
+                          // token is reduced, warm L2 with the next token's rows
 };
 
 // What a launch does with the prefix sum.
@@ -713,6 +714,20 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
 #pragma unroll
       for (int i = 0; i < N; ++i)
         v[i][k] = ok[k] ? ld_stream(p.bank + i * p.bank_stride + row + jj[k]) : z;
+    }
+    // While this token is reduced, let L2 fetch this CTA's rows of the next
+    // token it will take: the requests keep HBM busy during the reductions
+    // and the next loads hit L2.
+    if ((p.prefetch & 4) && m + static_cast<int>(gridDim.y) < p.M) {
+      constexpr int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3);
+      if (static_cast<int>(threadIdx.x) < rows && cend > c0) {
+        const int r = threadIdx.x;
+        const size_t off = static_cast<size_t>(m + gridDim.y) * p.H8 + c0;
+        const uint4* src = r < N ? p.bank + r * p.bank_stride + off
+                         : r == N ? p.prefix + off
+                         : r == N + 1 ? p.add + off : p.add2 + off;
+        prefetch_l2(src, static_cast<uint32_t>(cend - c0) * 16u);
+      }
     }
     // Let the next kernel on the stream be scheduled once every CTA of this
     // grid is past its loads; it still waits for this grid to finish.

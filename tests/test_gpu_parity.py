@@ -542,3 +542,15 @@ def test_cuda_graph_capture_and_replay():
         g.replay()
     torch.cuda.synchronize()
     assert (u16(newp) == ref_np).all() and (u16(out) == ref_out).all()
+
+
+@pytest.mark.parametrize("prefetch", [-1, 4, 5, 7])
+def test_next_token_prefetch_identical(prefetch):
+    """Clusters walking several tokens with the next token's rows prefetched
+    into L2 (bit 4): same bits as without, parity with the oracle."""
+    inp = wl.make_inputs(67, 12, H, seed=95)
+    cfg = binding.make_config("stream", cluster=7, grid_tokens=5, prefetch=prefetch)
+    got = run_gpu(inp, cfg)
+    ref = run_gpu(inp, binding.make_config("stream", cluster=7, grid_tokens=5, prefetch=-1))
+    assert (got[0] == ref[0]).all() and (got[1] == ref[1]).all()
+    assert_parity(inp, *got)
