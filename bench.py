@@ -452,40 +452,66 @@ def chain_benchmark(binding, wl, layers=25):
 
 def run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_ranks, ws):
     """The same metric through the public API with pinned host buffers: every
-    step copies the inputs host->device, calls the op, and copies both
-    outputs back, all on the launching stream inside the timed region."""
+    step copies its inputs host->device, calls the op, and copies both outputs
+    back, all inside the timed region.  Steps are pipelined the way a
+    streaming caller would run them: uploads on one copy stream, the op on
+    the compute stream, downloads on another, with two device buffer sets so
+    that step k+1's upload overlaps step k's download."""
     import torch
-    host = {k: getattr(inp, k).cpu().pin_memory() for k in ("prefix", "add", "add2", "bank", "w", "gamma")}
-    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    newp_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    dev = {k: torch.empty_like(getattr(inp, k)) for k in host}
+    keys = ("prefix", "add", "add2", "bank", "w", "gamma")
+    host = {k: getattr(inp, k).cpu().pin_memory() for k in keys}
+    dev = [{k: torch.empty_like(getattr(inp, k)) for k in keys} for _ in range(2)]
+    outs = [(torch.empty_like(out), torch.empty_like(newp)) for _ in range(2)]
+    host_outs = [(torch.empty(out.shape, dtype=out.dtype, pin_memory=True),
+                  torch.empty(out.shape, dtype=out.dtype, pin_memory=True)) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = 2 * out.numel() * out.element_size()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    uploaded = [ev(), ev()]
+    computed = [ev(), ev()]
+    downloaded = [ev(), ev()]
+    used = [False, False]
 
-    def e2e_step():
-        for k in host:
-            dev[k].copy_(host[k], non_blocking=True)
-        binding.attnres_add_rmsnorm(dev["prefix"], dev["add"], dev["add2"], dev["bank"], dev["w"],
-                                    dev["gamma"], inp.eps, out, newp, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        newp_h.copy_(newp, non_blocking=True)
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+    def step(k):
+        b = k % 2
+        with torch.cuda.stream(up):
+            if used[b]:
+                up.wait_event(computed[b])       # the op of step k-2 has read buffer set b
+            for key in keys:
+                dev[b][key].copy_(host[key], non_blocking=True)
+            uploaded[b].record(up)
+        with torch.cuda.stream(stream):
+            stream.wait_event(uploaded[b])
+            if used[b]:
+                stream.wait_event(downloaded[b])  # step k-2's outputs are on the host
+            d = dev[b]
+            binding.attnres_add_rmsnorm(d["prefix"], d["add"], d["add2"], d["bank"], d["w"],
+                                        d["gamma"], inp.eps, outs[b][0], outs[b][1], stream=stream)
+            computed[b].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(computed[b])
+            host_outs[b][0].copy_(outs[b][0], non_blocking=True)
+            host_outs[b][1].copy_(outs[b][1], non_blocking=True)
+            downloaded[b].record(down)
+        used[b] = True
+
+    for k in range(max(1, args.warmup)):
+        step(k)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            e2e_step()
-    e1.record(stream)
+    e0.record(up)
+    for k in range(args.steps):
+        step(k)
+    down.wait_event(downloaded[(args.steps - 1) % 2])
+    e1.record(down)
     barrier()
     e2e_s = max_ranks(e0.elapsed_time(e1) / 1e3)
     e2e_value = weak_scaling_value(nbytes, ws, args.steps, e2e_s)
-    del dev, host, out_h, newp_h
+    del dev, host, outs, host_outs
     return {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s / args.steps * 1e3, 3)}
-
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s / args.steps * 1e3, 3),
+            "pipelined": "uploads, op and downloads on three streams, two buffer sets"}
 
 
 def run_ours(args):
