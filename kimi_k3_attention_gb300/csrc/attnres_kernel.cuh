@@ -6,13 +6,16 @@
 // and keeps them in registers from the single HBM read to the final store:
 //
 //   load    prefix, add, add2, bank[0..N-1] chunks: 16-byte vector loads
-//           straight to registers (attnres_fused_kernel), or cp.async copies
-//           into a per-thread shared-memory ring several tokens ahead
-//           (attnres_pipe_kernel, persistent)
+//           straight to registers (attnres_fused_kernel; a cluster may walk
+//           several tokens and ask L2 for the next one's rows while it
+//           reduces the current one), or cp.async copies into a per-thread
+//           shared-memory ring several tokens ahead (attnres_pipe_kernel,
+//           persistent)
 //   fold    new_prefix = bf16(prefix + bf16(add + add2)) with add.rn.f32 and
 //           cvt.rn.bf16x2.f32 written in PTX, so no fast-math flag can turn
 //           them into flush-to-zero forms (TensorRT-LLM PR #20546, "Op")
-//   stats   ss_i = sum v^2 and d_i = w.v for the N+1 sources, one pass
+//   stats   ss_i = sum v^2 and d_i = w.v for the N+1 sources, one pass of
+//           mixed-precision FMAs (BF16 operands, float32 accumulators)
 //   R1      2(N+1) partial sums: warp transpose-reduction, CTA sum in shared
 //           memory, then every CTA stores its totals into the shared memory
 //           of every CTA of the cluster with st.async, each store counted on
@@ -24,11 +27,13 @@
 //   out     bf16(h * rsqrt(mean(h^2) + eps) * gamma) and new_prefix stored
 //
 // Every reduction has a fixed order, so results are deterministic.  Waits:
-// the CTA barrier, one cluster barrier at start-up (every thread of every CTA
-// reaches it on the same path), cp.async.wait_group (completes with its
-// copies), and the exchange mbarriers, whose waits are bounded in time: on
-// expiry the kernel sets a bit in the library's status word, stops waiting,
-// and stays resident for the same bound before exiting.
+// the CTA barrier, one cluster barrier per kernel (arrive when the exchange
+// mbarriers are set up, wait before the first remote store; every thread of
+// every CTA reaches both on the same path), cp.async.wait_group (completes
+// with its copies), griddepcontrol.wait (completes with the previous grid),
+// and the exchange mbarriers, whose waits are bounded in time: on expiry the
+// kernel sets a bit in the library's status word, stops waiting, and stays
+// resident for the same bound before exiting.
 #pragma once
 
 #include <cuda_runtime.h>
