@@ -60,7 +60,7 @@ typedef struct CUstream_st* attnres_stream_t;
 typedef enum {
   ATTNRES_OK = 0,
   ATTNRES_ERR_NULL = -1,    /* a required pointer is NULL                  */
-  ATTNRES_ERR_SHAPE = -2,   /* M < 1, N not in [0,12], H not a multiple of 8
+  ATTNRES_ERR_SHAPE = -2,   /* M < 1, N not in [0,31], H not a multiple of 8
                                or H outside [8, 16384]                     */
   ATTNRES_ERR_ALIGN = -3,   /* a pointer is not 16-byte aligned            */
   ATTNRES_ERR_ALIAS = -4,   /* out overlaps a tensor, or new_prefix overlaps
@@ -71,7 +71,7 @@ typedef enum {
   ATTNRES_ERR_CONFIG = -8   /* a forced launch configuration is invalid    */
 } attnres_status;
 
-#define ATTNRES_MAX_N 12   /* N = 0 is allowed */
+#define ATTNRES_MAX_N 31   /* N = 0 is allowed */
 #define ATTNRES_MAX_H 16384
 
 /*
@@ -81,7 +81,7 @@ typedef enum {
  *   add         [M,H]   first deferred addend (routed MoE output)
  *   add2        [M,H]   second addend (shared-expert output) or NULL: with
  *                       NULL the fold is new_prefix = bf16(prefix + add)
- *   bank        [N,M,H] depth bank of snapshots, 0 <= N <= 12 (may be NULL
+ *   bank        [N,M,H] depth bank of snapshots, 0 <= N <= 31 (may be NULL
  *                       when N = 0)
  *   w           [H]     per-layer pseudo-query of the mixture
  *   gamma       [H]     RMSNorm weight of the output norm
@@ -93,8 +93,10 @@ typedef enum {
  *
  * N = 0 ("no snapshots yet", the first layer) is supported: the new prefix is
  * the only source, alpha = 1 and out = RMSNorm(new_prefix) * gamma; the PR
- * adds first and runs another path there.  N > 12 is rejected with
- * ATTNRES_ERR_SHAPE (the PR's fused path also stops at 12 snapshots).
+ * adds first and runs another path there.  13 <= N <= 31 ("N > 12", the
+ * PR's other fallback) is fused here too, in variant 2 only; N > 31 is
+ * rejected with ATTNRES_ERR_SHAPE (the sums of 32 sources fill two warp-wide
+ * reductions).
  * The launch configuration is chosen from (M, N, H) and the SM count.
  */
 int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
@@ -112,6 +114,9 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *                 exchanged through distributed shared memory;
  *             3 = as 2 with at most 224 threads and registers capped so that
  *                 three CTAs share an SM;
+ *             Variants 1 and 4 exist for N <= 12 only.  For N > 12
+ *             variant 3 takes at most 128 threads, registers capped so
+ *             that three to five CTAs (fewer as N grows) share an SM.
  *             4 = persistent and pipelined (the large-M streaming kernel): a
  *                 grid of as many clusters as fit the GPU at once walks the
  *                 tokens; every thread copies its chunks of the token

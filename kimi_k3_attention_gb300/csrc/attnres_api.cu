@@ -9,6 +9,17 @@
 #include "attnres_launch.cuh"
 
 namespace attnres {
+
+// The kernels are compiled in the attnres_inst_*.cu units only.
+ATTNRES_UNIT_A(extern)
+ATTNRES_UNIT_B(extern)
+ATTNRES_UNIT_C(extern)
+ATTNRES_UNIT_D(extern)
+ATTNRES_UNIT_E(extern)
+ATTNRES_UNIT_F(extern)
+ATTNRES_UNIT_G(extern)
+ATTNRES_UNIT_H(extern)
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
@@ -136,11 +147,12 @@ int validate(const Args& a) {
 
 int round_up32(int x) { return (x + 31) & ~31; }
 
-// Fill every zero field of *c for (M, H) on a device with `sms` SMs, then
-// check the result.  Returns ATTNRES_OK or ATTNRES_ERR_CONFIG.
 // Dynamic shared memory the pipelined ring may take: the 227 KB a CTA can
 // hold, less the kernel's static exchange buffers and a little slack.
-constexpr size_t kPipeSmemMax = 227 * 1024 - sizeof(Exchange) - 1024;
+constexpr size_t kPipeSmemMax = 227 * 1024 - sizeof(Exchange<1>) - 1024;
+
+// Fill every zero field of *c for (M, N, H) on a device with `sms` SMs, then
+// check the result.  Returns ATTNRES_OK or ATTNRES_ERR_CONFIG.
 
 int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
   const int H8 = H / 8;
@@ -149,6 +161,11 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
     while (cl <= 16 && round_up32((H8 + cl - 1) / cl) > maxt) ++cl;
     return cl;
   };
+  // Deep banks (more than kShallowMaxN snapshots) have variants 2 and 3
+  // only, and a streaming shape of their own.
+  const bool deep = N > kShallowMaxN;
+  if (deep && (c->variant == 1 || c->variant == 4)) return ATTNRES_ERR_CONFIG;
+  const int stream_maxt = deep ? kDeepStreamMaxT : kStreamMaxT;
   if (c->variant == 0) {
     // Measured on GB300 at H = 7168 (the cluster sizes below are for that
     // H and scale with it): up to 32 tokens, a cluster of about 128 / M CTAs
@@ -156,12 +173,19 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
     // to 48 tokens, 8 CTAs of 112 columns (three fit an SM, still one
     // wave); then the register-capped shape, 4 CTAs of 224 columns up to 96
     // tokens and 7 CTAs of 128 columns beyond, where many tokens are in
-    // flight on every SM.
+    // flight on every SM.  Deep banks: up to 32 tokens the same clusters
+    // (4 CTAs from 8 tokens on once N >= 24, where a token's rows are many),
+    // beyond that their streaming shape, 7 CTAs of 128 columns (the split
+    // shape's CTAs hold too many registers to share an SM).
     int ref;
     if (M <= 32) {
       c->variant = 2;
       ref = (128 + M / 2) / M;
       ref = ref < 4 ? 4 : (ref > 8 ? 8 : ref);
+      if (N >= 24 && M >= 8) ref = 4;
+    } else if (deep) {
+      c->variant = 3;
+      ref = 7;
     } else if (M <= 48) {
       c->variant = 2;
       ref = 8;
@@ -173,7 +197,7 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
       ref = 7;
     }
     if (c->cluster == 0) {
-      const int lo = min_cluster(c->variant == 2 ? kSplitMaxT : kStreamMaxT);
+      const int lo = min_cluster(c->variant == 2 ? kSplitMaxT : stream_maxt);
       int cl = (ref * H8 + 448) / 896;
       c->cluster = cl < lo ? lo : (cl > 16 ? 16 : cl);
     }
@@ -186,7 +210,7 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
     if (c->threads < need || c->threads > kCtaMaxT || (c->threads % 32) != 0)
       return ATTNRES_ERR_CONFIG;
   } else if (c->variant == 2 || c->variant == 3) {
-    const int maxt = (c->variant == 2) ? kSplitMaxT : kStreamMaxT;
+    const int maxt = (c->variant == 2) ? kSplitMaxT : stream_maxt;
     if (c->cluster == 0) c->cluster = min_cluster(maxt);
     if (c->cluster < 1 || c->cluster > 16) return ATTNRES_ERR_CONFIG;
     const int cpc = (H8 + c->cluster - 1) / c->cluster;
@@ -208,10 +232,10 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
       // deepest that fits one
       c->stages = 4;
       while (c->stages > 2 &&
-             2 * (pipe_smem_bytes(N, add2, c->threads, c->stages) + sizeof(Exchange) + 1024) >
+             2 * (pipe_smem_bytes(N, add2, c->threads, c->stages) + sizeof(Exchange<1>) + 1024) >
                  228 * 1024)
         --c->stages;
-      if (2 * (pipe_smem_bytes(N, add2, c->threads, c->stages) + sizeof(Exchange) + 1024) >
+      if (2 * (pipe_smem_bytes(N, add2, c->threads, c->stages) + sizeof(Exchange<1>) + 1024) >
           228 * 1024) {
         c->stages = 4;
         while (c->stages > 2 && pipe_smem_bytes(N, add2, c->threads, c->stages) > kPipeSmemMax)
@@ -244,8 +268,9 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
   if (c->pdl == 0) c->pdl = 1;
   if (c->prefetch < -1 || c->prefetch > 7) return ATTNRES_ERR_CONFIG;
   if (c->prefetch == 0) {
-    c->prefetch = ((c->variant == 2 || c->variant == 3) && M <= 96) ? 1 : 0;
-    if (c->variant == 3 && c->grid_tokens < M) c->prefetch |= 4;   // clusters walk tokens
+    const bool fused = c->variant == 2 || c->variant == 3;
+    c->prefetch = (fused && M <= 96) ? 1 : 0;
+    if (fused && c->grid_tokens < M) c->prefetch |= 4;   // clusters walk tokens
     if (c->prefetch == 0) c->prefetch = -1;
   }
   if (c->prefetch > 0 && c->variant != 2 && c->variant != 3) return ATTNRES_ERR_CONFIG;
@@ -296,6 +321,37 @@ cudaError_t dispatch_pipe_stages(int stages, const Params& p, dim3 g, int t, int
     case 4: return launch_pipe<N, ADD2, 4>(p, g, t, c, pdl, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// Deep banks: the split shape (STREAM false) or the deep streaming shape,
+// with or without the fold.
+template <int N, bool STREAM>
+cudaError_t launch_deep(int mode, const Params& p, dim3 g, int t, int c, bool pdl,
+                        cudaStream_t s) {
+  constexpr int VPT = STREAM ? kStreamVPT : kSplitVPT;
+  constexpr int MAXT = STREAM ? kDeepStreamMaxT : kSplitMaxT;
+  constexpr int MINB = STREAM ? deep_minb(N) : kSplitMinB;
+  return mode == kFoldAdd2 ? launch_fused<N, kFoldAdd2, VPT, MAXT, MINB>(p, g, t, c, pdl, s)
+         : mode == kFoldAdd ? launch_fused<N, kFoldAdd, VPT, MAXT, MINB>(p, g, t, c, pdl, s)
+                            : launch_fused<N, kNoFold, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
+}
+
+template <bool STREAM>
+cudaError_t dispatch_deep(int N, int mode, const Params& p, dim3 g, int t, int c, bool pdl,
+                          cudaStream_t s) {
+#define ATTNRES_CASE(n) \
+  case n:               \
+    return launch_deep<n, STREAM>(mode, p, g, t, c, pdl, s);
+  switch (N) {
+    ATTNRES_CASE(13) ATTNRES_CASE(14) ATTNRES_CASE(15) ATTNRES_CASE(16)
+    ATTNRES_CASE(17) ATTNRES_CASE(18) ATTNRES_CASE(19) ATTNRES_CASE(20)
+    ATTNRES_CASE(21) ATTNRES_CASE(22) ATTNRES_CASE(23) ATTNRES_CASE(24)
+    ATTNRES_CASE(25) ATTNRES_CASE(26) ATTNRES_CASE(27) ATTNRES_CASE(28)
+    ATTNRES_CASE(29) ATTNRES_CASE(30) ATTNRES_CASE(31)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef ATTNRES_CASE
 }
 
 cudaError_t dispatch_pipe(int N, bool add2, int stages, const Params& p, dim3 g, int t, int c,
@@ -350,7 +406,12 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
   const bool pdl = c.pdl >= 0;
   cudaError_t e;
-  if (!a.fold && c.variant == 2)
+  const int mode = !a.fold ? kNoFold : has_add2 ? kFoldAdd2 : kFoldAdd;
+  if (a.N > kShallowMaxN && c.variant == 2)
+    e = dispatch_deep<false>(a.N, mode, p, grid, c.threads, c.cluster, pdl, s);
+  else if (a.N > kShallowMaxN)
+    e = dispatch_deep<true>(a.N, mode, p, grid, c.threads, c.cluster, pdl, s);
+  else if (!a.fold && c.variant == 2)
     e = dispatch_nofold<kSplitVPT, kSplitMaxT, kSplitMinB>(a.N, p, grid, c.threads, c.cluster, pdl, s);
   else if (!a.fold)
     e = dispatch_nofold<kStreamVPT, kStreamMaxT, kStreamMinB>(a.N, p, grid, c.threads, c.cluster,
@@ -481,7 +542,7 @@ extern "C" const char* attnres_status_string(int status) {
   switch (status) {
     case ATTNRES_OK: return "ok";
     case ATTNRES_ERR_NULL: return "a required pointer is NULL";
-    case ATTNRES_ERR_SHAPE: return "unsupported shape: need M >= 1, 0 <= N <= 12, 8 <= H <= 16384, H % 8 == 0";
+    case ATTNRES_ERR_SHAPE: return "unsupported shape: need M >= 1, 0 <= N <= 31, 8 <= H <= 16384, H % 8 == 0";
     case ATTNRES_ERR_ALIGN: return "a pointer is not 16-byte aligned";
     case ATTNRES_ERR_ALIAS: return "out overlaps a tensor, or new_prefix overlaps an input other than prefix";
     case ATTNRES_ERR_EPS: return "eps must be finite and > 0";

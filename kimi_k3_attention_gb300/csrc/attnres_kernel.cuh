@@ -318,6 +318,12 @@ __device__ __forceinline__ float half_warp_max(float v) {
   return v;
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+
 // Transpose-reduction of KP (a power of two <= 32) values per lane across the
 // warp with KP-1 + (5 - log2 KP) shuffles.  Afterwards lane l holds the warp
 // total of value index l >> (5 - log2 KP); lanes sharing an index agree.
@@ -349,6 +355,25 @@ struct Pow2 {
   static constexpr int log2 = K <= 2 ? 1 : K <= 4 ? 2 : K <= 8 ? 3 : K <= 16 ? 4 : 5;
 };
 
+// The 2(N+1) sums of a token (ss_i, d_i for every source, in source order)
+// are reduced in groups of up to 16 sources, one warp transpose-reduction of
+// at most 32 values each: one group for N <= 15, two for N <= 31.  Group g
+// is padded to KP<g> values; `total` floats per CTA cross the cluster.
+template <int N>
+struct Sums {
+  static constexpr int S = N + 1;
+  static constexpr int K = 2 * S;
+  static constexpr int G = (K + 31) / 32;
+  static constexpr int K0 = K < 32 ? K : 32;
+  static constexpr int K1 = K - K0;
+  static constexpr int KP0 = Pow2<K0>::value;
+  static constexpr int KP1 = K1 > 0 ? Pow2<K1>::value : 0;
+  static constexpr int SH0 = 5 - Pow2<K0>::log2;
+  static constexpr int SH1 = 5 - Pow2<(K1 > 0 ? K1 : 1)>::log2;
+  static constexpr int total = KP0 + KP1;
+  static_assert(G <= 2, "at most 31 bank snapshots");
+};
+
 // ---------------------------------------------------------------- per token
 
 // Shared memory of the per-token reductions.
@@ -357,8 +382,8 @@ struct Pow2 {
 //   xin2: per-warp sums of h^2 pushed by each CTA, index rank * warps + warp
 //   bar1, bar2: mbarriers counting the bytes of xin1 / xin2 of one token
 // Protocol per token k (phase parity k & 1 on both mbarriers):
-//   R1: warp 0 of every CTA stores its KP totals into xin1[rank] of every
-//       CTA with st.async; every thread waits on bar1; thread 0 then re-arms
+//   R1: warp 0 of every CTA stores its Sums<N>::total totals into
+//       xin1[rank] of every CTA with st.async; every thread waits on bar1; thread 0 then re-arms
 //       bar1 for token k+1.
 //   R2: lane c of every warp stores the warp's sum of h^2 into CTA c; every
 //       thread waits on bar2; thread 0 re-arms bar2.
@@ -369,10 +394,11 @@ struct Pow2 {
 // phase can complete while a local thread still waits on the previous one,
 // and the transaction count never runs ahead of its arming.  No CTA reads
 // another's shared memory, so there is no barrier at exit.
+template <int G>
 struct Exchange {
-  float red[16][32];     // up to 16 warps (448-thread CTAs have 14)
-  float xin1[16][32];    // up to 16 CTAs per cluster
-  float xin2[256];       // 16 CTAs x 16 warps
+  float red[16][32 * G];   // up to 16 warps (448-thread CTAs have 14)
+  float xin1[16][32 * G];  // up to 16 CTAs per cluster
+  float xin2[256];         // 16 CTAs x 16 warps
   unsigned long long bar1;
   unsigned long long bar2;
 };
@@ -384,8 +410,8 @@ struct Thread {
   bool failed;      // an exchange wait timed out: stop waiting, report it
 };
 
-// Bytes each CTA expects per token: KP totals from every CTA (R1) and one
-// float per warp of every CTA (R2).
+// Bytes each CTA expects per token: kp (Sums<N>::total) totals from every
+// CTA (R1) and one float per warp of every CTA (R2).
 __device__ __forceinline__ uint32_t r1_bytes(int kp, const Thread& t, const Params& p) {
   return static_cast<uint32_t>(kp) * t.csize * 4u + p.extra_tx;
 }
@@ -397,8 +423,8 @@ __device__ __forceinline__ uint32_t r2_bytes(const Thread& t, const Params& p) {
 // both mbarriers; the start of the cluster handshake (arrive now, wait
 // before the first remote store) both publishes them and guarantees every
 // CTA of the cluster runs.
-template <int KP>
-__device__ __forceinline__ void exchange_init(Exchange& x, const Thread& t, const Params& p) {
+template <int KP, int G>
+__device__ __forceinline__ void exchange_init(Exchange<G>& x, const Thread& t, const Params& p) {
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&x.bar1), 1);
     mbar_init(smem_u32(&x.bar2), 1);
@@ -464,34 +490,14 @@ struct SmemSources {
   __device__ __forceinline__ void fence() {}
 };
 
-// Everything after the loads for one token: fold, sums, both exchanges,
-// softmax, mixture, and the two stores.  pr/ad/ad2 are the token's prefix and
-// addend chunks, src gives the bank chunks (and receives the updated prefix),
-// wv the pseudo-query chunks; masked chunks (ok false) are zeros and store
-// nothing.
-template <int N, int MODE, int VPT, class Src>
-__device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thread& t,
-                                               size_t row, const int (&jj)[VPT],
-                                               const bool (&ok)[VPT], const uint4 (&wv)[VPT],
-                                               const uint4 (&gv)[VPT],
-                                               const uint4 (&pr)[VPT], const uint4 (&ad)[VPT],
-                                               const uint4 (&ad2)[VPT], Src& src, bool& first) {
-  constexpr int S = N + 1;             // sources: bank[0..N-1], new prefix
-  constexpr int K = 2 * S;             // per-token sums: (ss_i, d_i)
-  constexpr int KP = Pow2<K>::value;
-  constexpr int SHIFT = 5 - Pow2<K>::log2;
-  const int lane = t.lane, warp = t.warp;
-
-  // ---- fold (the updated prefix is stored at the end: a global store in
-  // flight would make the release barriers below wait for it)
+// Sums of squares and dot products with w of sources I0..I1-1 over this
+// thread's chunks: part[2(i - I0)] = ss_i, part[2(i - I0) + 1] = d_i, the
+// rest of the KP slots zero.
+template <int I0, int I1, int KP, int VPT, class Src>
+__device__ __forceinline__ void source_sums(const Src& src, const uint4 (&wv)[VPT],
+                                            float (&part)[KP]) {
 #pragma unroll
-  for (int k = 0; k < VPT; ++k)
-    src.set_new_prefix(k, MODE == kNoFold ? pr[k] : fold_chunk<MODE == kFoldAdd2>(pr[k], ad[k], ad2[k]));
-
-  // ---- per-source sums of squares and dot products with w
-  float part[KP];
-#pragma unroll
-  for (int i = 0; i < S; ++i) {
+  for (int i = I0; i < I1; ++i) {
     float ss = 0.f, d = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -501,16 +507,56 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
       stats_word(u.z, wv[k].z, ss, d);
       stats_word(u.w, wv[k].w, ss, d);
     }
-    part[2 * i] = ss;
-    part[2 * i + 1] = d;
+    part[2 * (i - I0)] = ss;
+    part[2 * (i - I0) + 1] = d;
   }
 #pragma unroll
-  for (int i = K; i < KP; ++i) part[i] = 0.f;
-  src.fence();
+  for (int i = 2 * (I1 - I0); i < KP; ++i) part[i] = 0.f;
+}
 
-  // ---- R1: warp transpose-reduction, CTA sum, st.async to every CTA
-  const float wtot = warp_transpose_reduce<KP>(part, lane);
-  if ((lane & ((1 << SHIFT) - 1)) == 0) x.red[warp][lane >> SHIFT] = wtot;
+// Everything after the loads for one token: fold, sums, both exchanges,
+// softmax, mixture, and the two stores.  pr/ad/ad2 are the token's prefix and
+// addend chunks, src gives the bank chunks (and receives the updated prefix),
+// wv the pseudo-query chunks; masked chunks (ok false) are zeros and store
+// nothing.
+template <int N, int MODE, int VPT, class Src>
+__device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>::G>& x, Thread& t,
+                                               size_t row, const int (&jj)[VPT],
+                                               const bool (&ok)[VPT], const uint4 (&wv)[VPT],
+                                               const uint4 (&gv)[VPT],
+                                               const uint4 (&pr)[VPT], const uint4 (&ad)[VPT],
+                                               const uint4 (&ad2)[VPT], Src& src, bool& first) {
+  using SL = Sums<N>;
+  constexpr int S = SL::S;             // sources: bank[0..N-1], new prefix
+  constexpr int S0 = S < 16 ? S : 16;  // sources of the first group
+  const int lane = t.lane, warp = t.warp;
+
+  // ---- fold (the updated prefix is stored at the end: a global store in
+  // flight would make the release barriers below wait for it)
+#pragma unroll
+  for (int k = 0; k < VPT; ++k)
+    src.set_new_prefix(k, MODE == kNoFold ? pr[k] : fold_chunk<MODE == kFoldAdd2>(pr[k], ad[k], ad2[k]));
+
+  // ---- per-source sums of squares and dot products with w, and R1: warp
+  // transpose-reduction per group, CTA sum, st.async to every CTA
+  float wt0, wt1 = 0.f;
+  {
+    float part0[SL::KP0];
+    source_sums<0, S0>(src, wv, part0);
+    if constexpr (SL::G == 1) {
+      src.fence();
+      wt0 = warp_transpose_reduce<SL::KP0>(part0, lane);
+    } else {
+      wt0 = warp_transpose_reduce<SL::KP0>(part0, lane);
+      float part1[SL::KP1 > 0 ? SL::KP1 : 1];
+      source_sums<16, S>(src, wv, part1);
+      src.fence();
+      wt1 = warp_transpose_reduce<SL::KP1>(part1, lane);
+    }
+  }
+  if ((lane & ((1 << SL::SH0) - 1)) == 0) x.red[warp][lane >> SL::SH0] = wt0;
+  if constexpr (SL::G == 2)
+    if ((lane & ((1 << SL::SH1) - 1)) == 0) x.red[warp][32 + (lane >> SL::SH1)] = wt1;
   __syncthreads();
   const uint32_t bar1 = smem_u32(&x.bar1), bar2 = smem_u32(&x.bar2);
   // The first remote store of the kernel waits for every CTA of the cluster
@@ -519,31 +565,52 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
     cluster_wait();
     first = false;
   }
-  if (warp == 0 && lane < KP) {
-    float s = 0.f;
+  if (warp == 0) {
 #pragma unroll
-    for (int w = 0; w < 16; ++w)
-      if (w < t.nwarps) s += x.red[w][lane];
-    const uint32_t a = smem_u32(&x.xin1[t.crank][lane]);
-    for (uint32_t c = 0; c < t.csize; ++c) st_async_f32(dsmem_map(a, c), s, dsmem_map(bar1, c));
+    for (int g = 0; g < SL::G; ++g) {
+      const int kp = g == 0 ? SL::KP0 : SL::KP1;
+      if (lane < kp) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < 16; ++w)
+          if (w < t.nwarps) s += x.red[w][32 * g + lane];
+        const uint32_t a = smem_u32(&x.xin1[t.crank][32 * g + lane]);
+        for (uint32_t c = 0; c < t.csize; ++c) st_async_f32(dsmem_map(a, c), s, dsmem_map(bar1, c));
+      }
+    }
   }
   exchange_wait(bar1, t, p);
-  if (threadIdx.x == 0 && !t.failed) mbar_arm(bar1, r1_bytes(KP, t, p));  // next token
-  float tot = 0.f;
-  if (lane < KP) {
+  if (threadIdx.x == 0 && !t.failed) mbar_arm(bar1, r1_bytes(SL::total, t, p));  // next token
+  // cluster totals: lane l of tot[g] holds sum 32 g + l
+  float tot[SL::G];
 #pragma unroll
-    for (uint32_t c = 0; c < 16; ++c)
-      if (c < t.csize) tot += x.xin1[c][lane];
+  for (int g = 0; g < SL::G; ++g) {
+    const int kp = g == 0 ? SL::KP0 : SL::KP1;
+    tot[g] = 0.f;
+    if (lane < kp) {
+#pragma unroll
+      for (uint32_t c = 0; c < 16; ++c)
+        if (c < t.csize) tot[g] += x.xin1[c][32 * g + lane];
+    }
   }
 
-  // ---- logits and softmax, lane i < S holds source i
-  const float ss_i = __shfl_sync(FULL, tot, (2 * lane) & 31);
-  const float d_i = __shfl_sync(FULL, tot, (2 * lane + 1) & 31);
+  // ---- logits and softmax, lane i < S holds source i (sums 2i and 2i + 1
+  // sit in group i / 16 at lanes (2i) mod 32 and (2i + 1) mod 32)
+  float ss_i = __shfl_sync(FULL, tot[0], (2 * lane) & 31);
+  float d_i = __shfl_sync(FULL, tot[0], (2 * lane + 1) & 31);
+  if constexpr (SL::G == 2) {
+    const float ss1 = __shfl_sync(FULL, tot[SL::G - 1], (2 * lane) & 31);
+    const float d1 = __shfl_sync(FULL, tot[SL::G - 1], (2 * lane + 1) & 31);
+    if (lane >= 16) {
+      ss_i = ss1;
+      d_i = d1;
+    }
+  }
   const float logit = (lane < S) ? rsqrtf(__fmaf_rn(ss_i, p.inv_h, p.eps)) * d_i : -INFINITY;
-  // S <= 13 sources sit in lanes 0..15: reduce over 16 lanes
-  const float mx = half_warp_max(logit);
+  // up to 16 sources sit in lanes 0..15: reduce over 16 lanes, else 32
+  const float mx = S <= 16 ? half_warp_max(logit) : warp_max(logit);
   const float ex = (lane < S) ? __expf(logit - mx) : 0.f;
-  const float den = half_warp_sum(ex);
+  const float den = S <= 16 ? half_warp_sum(ex) : warp_sum(ex);
   const float alpha_l = ex / den;
   float alpha[S];
 #pragma unroll
@@ -611,10 +678,6 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange& x, Thr
   }
 }
 
-template <int N>
-struct KPOf {
-  static constexpr int value = Pow2<2 * (N + 1)>::value;
-};
 
 __device__ __forceinline__ Thread thread_info() {
   Thread t;
@@ -634,7 +697,7 @@ __device__ __forceinline__ Thread thread_info() {
 // blockIdx.y + gridDim.y, ...
 template <int N, int MODE, int VPT, int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params p) {
-  __shared__ Exchange x;
+  __shared__ Exchange<Sums<N>::G> x;
   Thread t = thread_info();
   const int c0 = static_cast<int>(t.crank) * p.cpc;
   const int cend = min(c0 + p.cpc, p.H8);
@@ -653,8 +716,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   if (p.prefetch & 2) griddep_launch_dependents();
   if (p.prefetch & 1) {
     const int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3) + 2;
-    if (static_cast<int>(threadIdx.x) < rows && cend > c0 && blockIdx.y < p.M) {
-      const int r = threadIdx.x;
+    for (int r = threadIdx.x; r < rows && cend > c0 && blockIdx.y < p.M; r += blockDim.x) {
       const size_t off = static_cast<size_t>(blockIdx.y) * p.H8 + c0;
       const uint32_t bytes = static_cast<uint32_t>(cend - c0) * 16u;
       const uint4* src = r < N ? p.bank + r * p.bank_stride + off
@@ -672,7 +734,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // streaming regime after the first token's loads are issued, so that the
   // set-up does not delay them.
   const bool early_init = p.prefetch != 0;
-  if (early_init && blockIdx.y < p.M) exchange_init<KPOf<N>::value>(x, t, p);
+  if (early_init && blockIdx.y < p.M) exchange_init<Sums<N>::total>(x, t, p);
   // Programmatic dependent launch: this grid may have been scheduled while
   // the previous kernel on the stream was still running; wait for it to
   // complete (and its writes to be visible) before reading its outputs.
@@ -706,8 +768,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // and the next loads hit L2.
     if ((p.prefetch & 4) && m + static_cast<int>(gridDim.y) < p.M) {
       constexpr int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3);
-      if (static_cast<int>(threadIdx.x) < rows && cend > c0) {
-        const int r = threadIdx.x;
+      for (int r = threadIdx.x; r < rows && cend > c0; r += blockDim.x) {
         const size_t off = static_cast<size_t>(m + gridDim.y) * p.H8 + c0;
         const uint4* src = r < N ? p.bank + r * p.bank_stride + off
                          : r == N ? p.prefix + off
@@ -718,7 +779,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // Let the next kernel on the stream be scheduled once every CTA of this
     // grid is past its loads; it still waits for this grid to finish.
     griddep_launch_dependents();
-    if (!early_init && m == static_cast<int>(blockIdx.y)) exchange_init<KPOf<N>::value>(x, t, p);
+    if (!early_init && m == static_cast<int>(blockIdx.y)) exchange_init<Sums<N>::total>(x, t, p);
     RegSources<N, VPT> src{v};
     token_epilogue<N, MODE, VPT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
   }
@@ -737,7 +798,7 @@ template <int N, bool ADD2, int MAXT, int MINB, int STAGES>
 __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p) {
   constexpr int ROWS = N + (ADD2 ? 3 : 2);   // prefix, add, [add2], bank[0..N-1]
   extern __shared__ uint4 ring[];             // [STAGES][ROWS][blockDim.x]
-  __shared__ Exchange x;
+  __shared__ Exchange<Sums<N>::G> x;
   Thread t = thread_info();
   const int c0 = static_cast<int>(t.crank) * p.cpc;
   const int cend = min(c0 + p.cpc, p.H8);
@@ -748,7 +809,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
   const uint32_t row_step = blockDim.x * 16u;
   const uint32_t stage_step = ROWS * row_step;
 
-  exchange_init<KPOf<N>::value>(x, t, p);
+  exchange_init<Sums<N>::total>(x, t, p);
   griddep_wait();
   const uint4 wv[1] = {ok[0] ? ld_keep(p.w + jj1) : make_uint4(0, 0, 0, 0)};
   const uint4 gv[1] = {ok[0] ? ld_keep(p.gamma + jj1) : make_uint4(0, 0, 0, 0)};

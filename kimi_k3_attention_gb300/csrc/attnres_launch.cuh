@@ -19,6 +19,15 @@ constexpr int kSplitVPT = 1, kSplitMaxT = 256, kSplitMinB = 1;
 constexpr int kStreamVPT = 1, kStreamMaxT = 224, kStreamMinB = 3;
 constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 
+// Every shape is compiled for N <= kShallowMaxN.  Deeper banks (up to
+// ATTNRES_MAX_N) have the split shape and a streaming shape of their own:
+// up to 128 threads, registers capped so that deep_minb(N) CTAs share an SM
+// (GB300, M = 8192: 4.7-6.1 TB/s for N = 13..31 against 3.3-4.1 TB/s
+// uncapped; spills stay within a few dozen bytes).
+constexpr int kShallowMaxN = 12;
+constexpr int kDeepStreamMaxT = 128;
+constexpr int deep_minb(int n) { return n <= 16 ? 5 : n <= 24 ? 4 : 3; }
+
 template <int N, int MODE, int VPT, int MAXT, int MINB>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
                          cudaStream_t s) {
@@ -146,31 +155,87 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
                             chunks);
 }
 
-#define ATTNRES_INSTANTIATE_PIPE(N, ADD2)                                                    \
-  template cudaError_t launch_pipe<N, ADD2, 2>(const Params&, dim3, int, int, bool,          \
-                                               cudaStream_t);                                \
-  template cudaError_t launch_pipe<N, ADD2, 3>(const Params&, dim3, int, int, bool,          \
-                                               cudaStream_t);                                \
-  template cudaError_t launch_pipe<N, ADD2, 4>(const Params&, dim3, int, int, bool,          \
-                                               cudaStream_t);
+// Instantiations.  Each attnres_inst_*.cu unit expands its share with DEF
+// empty (explicit instantiation definitions, where the kernels are
+// compiled); the API unit expands all of them with DEF = extern, so that it
+// compiles no kernel itself.
+#define ATTNRES_FUSED(DEF, N, MODE, VPT, MAXT, MINB)                                      \
+  DEF template cudaError_t launch_fused<N, MODE, VPT, MAXT, MINB>(const Params&, dim3, int, \
+                                                                  int, bool, cudaStream_t);
 
-#define ATTNRES_INSTANTIATE(N, ADD2)                                                       \
-  template cudaError_t launch_fused<N, ADD2 ? kFoldAdd2 : kFoldAdd, kSplitVPT, kSplitMaxT,     \
-                                    kSplitMinB>(const Params&, dim3, int, int, bool,         \
-                                                cudaStream_t);                               \
-  template cudaError_t launch_fused<N, ADD2 ? kFoldAdd2 : kFoldAdd, kStreamVPT, kStreamMaxT,   \
-                                    kStreamMinB>(const Params&, dim3, int, int, bool,        \
-                                                 cudaStream_t);                              \
-  template cudaError_t launch_fused<N, ADD2 ? kFoldAdd2 : kFoldAdd, kCtaVPT, kCtaMaxT,         \
-                                    kCtaMinB>(const Params&, dim3, int, int, bool,           \
-                                              cudaStream_t);                                 \
-  ATTNRES_INSTANTIATE_PIPE(N, ADD2)
+#define ATTNRES_PIPE(DEF, N, ADD2, STAGES)                                          \
+  DEF template cudaError_t launch_pipe<N, ADD2, STAGES>(const Params&, dim3, int, int, bool, \
+                                                        cudaStream_t);
 
-// The attention-residual + RMSNorm alone (no fold): split and streaming shapes.
-#define ATTNRES_INSTANTIATE_NOFOLD(N)                                                        \
-  template cudaError_t launch_fused<N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB>(          \
-      const Params&, dim3, int, int, bool, cudaStream_t);                                    \
-  template cudaError_t launch_fused<N, kNoFold, kStreamVPT, kStreamMaxT, kStreamMinB>(       \
-      const Params&, dim3, int, int, bool, cudaStream_t);
+// N <= 12 with the fold (add2 present or not): every shape.
+#define ATTNRES_INSTANTIATE(DEF, N, ADD2)                                                   \
+  ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB)     \
+  ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kStreamVPT, kStreamMaxT, kStreamMinB)  \
+  ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kCtaVPT, kCtaMaxT, kCtaMinB)           \
+  ATTNRES_PIPE(DEF, N, ADD2, 2)                                                             \
+  ATTNRES_PIPE(DEF, N, ADD2, 3)                                                             \
+  ATTNRES_PIPE(DEF, N, ADD2, 4)
+
+// The attention-residual + RMSNorm alone (no fold), N <= 12: split and
+// streaming shapes.
+#define ATTNRES_INSTANTIATE_NOFOLD(DEF, N)                               \
+  ATTNRES_FUSED(DEF, N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB)      \
+  ATTNRES_FUSED(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, kStreamMinB)
+
+// Deep banks, 13 <= N <= 31: the split shape and the deep streaming shape,
+// with the fold (add2 present or not) and without.
+#define ATTNRES_INSTANTIATE_DEEP(DEF, N)                                           \
+  ATTNRES_FUSED(DEF, N, kFoldAdd2, kSplitVPT, kSplitMaxT, kSplitMinB)              \
+  ATTNRES_FUSED(DEF, N, kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB)               \
+  ATTNRES_FUSED(DEF, N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB)                \
+  ATTNRES_FUSED(DEF, N, kFoldAdd2, kStreamVPT, kDeepStreamMaxT, deep_minb(N))      \
+  ATTNRES_FUSED(DEF, N, kFoldAdd, kStreamVPT, kDeepStreamMaxT, deep_minb(N))       \
+  ATTNRES_FUSED(DEF, N, kNoFold, kStreamVPT, kDeepStreamMaxT, deep_minb(N))
+
+#define ATTNRES_INSTANTIATE_TAIL_ADD(DEF)                                                  \
+  DEF template cudaError_t launch_tail_add<true>(const uint4*, const uint4*, const uint4*,  \
+                                                 uint4*, long long, int, bool, cudaStream_t); \
+  DEF template cudaError_t launch_tail_add<false>(const uint4*, const uint4*, const uint4*, \
+                                                  uint4*, long long, int, bool, cudaStream_t);
+
+// Which unit defines what.
+#define ATTNRES_UNIT_A(DEF)                                                             \
+  ATTNRES_INSTANTIATE(DEF, 1, true) ATTNRES_INSTANTIATE(DEF, 2, true)                   \
+  ATTNRES_INSTANTIATE(DEF, 3, true) ATTNRES_INSTANTIATE(DEF, 4, true)                   \
+  ATTNRES_INSTANTIATE(DEF, 5, true) ATTNRES_INSTANTIATE(DEF, 6, true)
+#define ATTNRES_UNIT_B(DEF)                                                             \
+  ATTNRES_INSTANTIATE(DEF, 7, true) ATTNRES_INSTANTIATE(DEF, 8, true)                   \
+  ATTNRES_INSTANTIATE(DEF, 9, true) ATTNRES_INSTANTIATE(DEF, 10, true)                  \
+  ATTNRES_INSTANTIATE(DEF, 11, true) ATTNRES_INSTANTIATE(DEF, 12, true)
+#define ATTNRES_UNIT_C(DEF)                                                             \
+  ATTNRES_INSTANTIATE(DEF, 1, false) ATTNRES_INSTANTIATE(DEF, 2, false)                 \
+  ATTNRES_INSTANTIATE(DEF, 3, false) ATTNRES_INSTANTIATE(DEF, 4, false)                 \
+  ATTNRES_INSTANTIATE(DEF, 5, false) ATTNRES_INSTANTIATE(DEF, 6, false)
+#define ATTNRES_UNIT_D(DEF)                                                             \
+  ATTNRES_INSTANTIATE(DEF, 7, false) ATTNRES_INSTANTIATE(DEF, 8, false)                 \
+  ATTNRES_INSTANTIATE(DEF, 9, false) ATTNRES_INSTANTIATE(DEF, 10, false)                \
+  ATTNRES_INSTANTIATE(DEF, 11, false) ATTNRES_INSTANTIATE(DEF, 12, false)
+#define ATTNRES_UNIT_E(DEF)                                                             \
+  ATTNRES_INSTANTIATE(DEF, 0, true) ATTNRES_INSTANTIATE(DEF, 0, false)                  \
+  ATTNRES_INSTANTIATE_NOFOLD(DEF, 0) ATTNRES_INSTANTIATE_NOFOLD(DEF, 1)                 \
+  ATTNRES_INSTANTIATE_NOFOLD(DEF, 2) ATTNRES_INSTANTIATE_NOFOLD(DEF, 3)                 \
+  ATTNRES_INSTANTIATE_NOFOLD(DEF, 4) ATTNRES_INSTANTIATE_NOFOLD(DEF, 5)                 \
+  ATTNRES_INSTANTIATE_NOFOLD(DEF, 6) ATTNRES_INSTANTIATE_NOFOLD(DEF, 7)                 \
+  ATTNRES_INSTANTIATE_NOFOLD(DEF, 8) ATTNRES_INSTANTIATE_NOFOLD(DEF, 9)                 \
+  ATTNRES_INSTANTIATE_NOFOLD(DEF, 10) ATTNRES_INSTANTIATE_NOFOLD(DEF, 11)               \
+  ATTNRES_INSTANTIATE_NOFOLD(DEF, 12) ATTNRES_INSTANTIATE_TAIL_ADD(DEF)
+#define ATTNRES_UNIT_F(DEF)                                                             \
+  ATTNRES_INSTANTIATE_DEEP(DEF, 13) ATTNRES_INSTANTIATE_DEEP(DEF, 14)                   \
+  ATTNRES_INSTANTIATE_DEEP(DEF, 15) ATTNRES_INSTANTIATE_DEEP(DEF, 16)                   \
+  ATTNRES_INSTANTIATE_DEEP(DEF, 17) ATTNRES_INSTANTIATE_DEEP(DEF, 18)
+#define ATTNRES_UNIT_G(DEF)                                                             \
+  ATTNRES_INSTANTIATE_DEEP(DEF, 19) ATTNRES_INSTANTIATE_DEEP(DEF, 20)                   \
+  ATTNRES_INSTANTIATE_DEEP(DEF, 21) ATTNRES_INSTANTIATE_DEEP(DEF, 22)                   \
+  ATTNRES_INSTANTIATE_DEEP(DEF, 23) ATTNRES_INSTANTIATE_DEEP(DEF, 24)
+#define ATTNRES_UNIT_H(DEF)                                                             \
+  ATTNRES_INSTANTIATE_DEEP(DEF, 25) ATTNRES_INSTANTIATE_DEEP(DEF, 26)                   \
+  ATTNRES_INSTANTIATE_DEEP(DEF, 27) ATTNRES_INSTANTIATE_DEEP(DEF, 28)                   \
+  ATTNRES_INSTANTIATE_DEEP(DEF, 29) ATTNRES_INSTANTIATE_DEEP(DEF, 30)                   \
+  ATTNRES_INSTANTIATE_DEEP(DEF, 31)
 
 }  // namespace attnres

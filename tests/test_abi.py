@@ -67,7 +67,7 @@ def _call(**kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(prefix=0), -1), (dict(add=0), -1), (dict(bank=0), -1), (dict(w=0), -1),
     (dict(gamma=0), -1), (dict(out=0), -1), (dict(new_prefix=0), -1),
-    (dict(N=-1), -2), (dict(N=13), -2), (dict(M=0), -2), (dict(H=12), -2), (dict(H=0), -2),
+    (dict(N=-1), -2), (dict(N=32), -2), (dict(M=0), -2), (dict(H=12), -2), (dict(H=0), -2),
     (dict(H=16392), -2),
     (dict(eps=0.0), -5), (dict(eps=-1e-6), -5), (dict(eps=float("inf")), -5), (dict(eps=float("nan")), -5),
     (dict(prefix=BASE + 8), -3), (dict(bank=BASE + (1 << 20) + 2), -3), (dict(out=BASE + (9 << 20) + 4), -3),
@@ -115,7 +115,7 @@ def test_new_entry_points_validate_on_host():
     assert lib.attnres_rmsnorm(vp(a["prefix"]), vp(a["bank"]), vp(a["w"]), vp(a["gamma"]), 1e-6,
                                vp(a["bank"] + 64), M, N, H, None) == -4
     assert lib.attnres_rmsnorm(vp(a["prefix"]), vp(a["bank"]), vp(a["w"]), vp(a["gamma"]), 1e-6,
-                               vp(a["out"]), M, 13, H, None) == -2
+                               vp(a["out"]), M, 32, H, None) == -2
     # N = 0 needs no bank, but N > 0 does
     assert lib.attnres_rmsnorm(vp(a["prefix"]), None, vp(a["w"]), vp(a["gamma"]), 1e-6,
                                vp(a["out"]), M, 1, H, None) == -1

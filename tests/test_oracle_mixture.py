@@ -95,13 +95,13 @@ def test_zero_query_gives_mean_of_sources():
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-15)
 
 
-@pytest.mark.parametrize("k", [0, 2, 5])
-def test_dominant_source_selected(k):
+@pytest.mark.parametrize("k,N", [(0, 5), (2, 5), (5, 5), (17, 31), (31, 31)])
+def test_dominant_source_selected(k, N):
     """w = 1 * v_k: l_k ~ H * rms(v_k) while the other logits are O(sqrt H), so
-    alpha -> e_k and out -> rms_norm(v_k) * gamma.  Source 5 is the updated
-    prefix (N = 5).  A flipped logit sign would select the opposite end."""
-    rng = np.random.default_rng(12 + k)
-    H, N = 256, 5
+    alpha -> e_k and out -> rms_norm(v_k) * gamma.  Source N is the updated
+    prefix.  A flipped logit sign would select the opposite end."""
+    rng = np.random.default_rng(12 + k + N)
+    H = 256
     bank = _rand_bf16(rng, (N, 1, H))
     prefix = _rand_bf16(rng, (1, H))
     add = _rand_bf16(rng, (1, H))
@@ -180,7 +180,7 @@ def _mp_reference(src, w, gamma, eps):
     return np.array([float(h[j] * rh * mpmath.mpf(float(gamma[j]))) for j in range(H)])
 
 
-@pytest.mark.parametrize("H,N,M", [(8, 1, 2), (16, 2, 3), (8, 12, 1)])
+@pytest.mark.parametrize("H,N,M", [(8, 1, 2), (16, 2, 3), (8, 12, 1), (8, 20, 1), (16, 31, 1)])
 def test_brute_force_high_precision(H, N, M):
     rng = np.random.default_rng(100 + H + N)
     bank = _rand_bf16(rng, (N, M, H))
