@@ -37,14 +37,25 @@ Arithmetic of the oracle:
   * The mixture and the output norm are evaluated in float64 and NOT rounded:
     the float64 `out` is compared against the GPU's BF16 output within a
     tolerance (see oracle/tolerance.py).
+  * FP16 tensors (fmt="fp16", IEEE binary16) take the same steps with the
+    FP16 codec: the PR's fused window is BF16 (section "Model"), and the same
+    op on a model kept in FP16 is read as every tensor and both fold
+    roundings in FP16.
 """
 from __future__ import annotations
 
 import numpy as np
 
 __all__ = [
+    "Format",
+    "BF16",
+    "FP16",
+    "decode",
+    "encode_rne",
     "bf16_decode",
     "bf16_encode_rne",
+    "fp16_decode",
+    "fp16_encode_rne",
     "fold",
     "mixture",
     "attnres_add_rmsnorm",
@@ -52,46 +63,71 @@ __all__ = [
     "algorithmic_bytes",
 ]
 
-_BF16_MAX_FINITE = (2.0 - 2.0 ** -7) * 2.0 ** 127
-# Values at or above this magnitude round (to nearest even) to infinity: the
-# midpoint between the largest finite BF16 and 2^128, and the largest finite
-# value's last mantissa bit is odd, so the tie goes up.
-_BF16_OVERFLOW = (2.0 - 2.0 ** -8) * 2.0 ** 127
-_BF16_MIN_NORMAL = 2.0 ** -126
-_BF16_SUBNORMAL_QUANTUM = 2.0 ** -133
-_BF16_QNAN = np.uint16(0x7FC0)
+class Format:
+    """A binary 16-bit floating-point format: 1 sign bit, `ebits` exponent bits
+    (bias 2^(ebits-1) - 1), `mbits` mantissa bits, IEEE-style subnormals,
+    infinities and NaNs.  BF16 is (8, 7); FP16 (IEEE binary16) is (5, 10)."""
+
+    def __init__(self, name, ebits, mbits):
+        self.name, self.ebits, self.mbits = name, ebits, mbits
+        self.bias = (1 << (ebits - 1)) - 1
+        self.emax = (1 << ebits) - 2 - self.bias              # largest normal exponent
+        self.min_normal = 2.0 ** (1 - self.bias)
+        self.sub_exp = 1 - self.bias - mbits                  # subnormal quantum 2^sub_exp
+        self.max_finite = (2.0 - 2.0 ** -mbits) * 2.0 ** self.emax
+        # Values at or above this magnitude round (to nearest even) to
+        # infinity: the midpoint between the largest finite value and
+        # 2^(emax+1); the largest finite value's last mantissa bit is odd, so
+        # the tie goes up.
+        self.overflow = (2.0 - 2.0 ** -(mbits + 1)) * 2.0 ** self.emax
+        self.exp_mask = (1 << ebits) - 1
+        self.inf_bits = self.exp_mask << mbits
+        self.qnan_bits = self.inf_bits | (1 << (mbits - 1))
 
 
-def bf16_decode(bits) -> np.ndarray:
-    """BF16 bit patterns (uint16) -> exact float64 values.
+BF16 = Format("bf16", 8, 7)
+FP16 = Format("fp16", 5, 10)
+FORMATS = {"bf16": BF16, "fp16": FP16}
 
-    Layout: 1 sign bit, 8 exponent bits (bias 127), 7 mantissa bits.
-    Exponent 0 encodes zero and subnormals (mantissa * 2^-133); exponent 255
-    encodes infinities (mantissa 0) and NaN (mantissa != 0).
+
+def _fmt(fmt) -> Format:
+    return fmt if isinstance(fmt, Format) else FORMATS[fmt]
+
+
+def decode(bits, fmt="bf16") -> np.ndarray:
+    """16-bit bit patterns (uint16) of format `fmt` -> exact float64 values.
+
+    Exponent field 0 encodes zero and subnormals (mantissa * 2^sub_exp); the
+    all-ones exponent encodes infinities (mantissa 0) and NaN (mantissa != 0);
+    otherwise the value is 1.mantissa * 2^(exponent - bias).
     """
+    f = _fmt(fmt)
     u = np.asarray(bits, dtype=np.uint16).astype(np.int64)
     sign = (u >> 15) & 1
-    e = (u >> 7) & 0xFF
-    m = u & 0x7F
-    normal_sig = (m + 128).astype(np.float64)          # 1.m as an integer * 2^7
+    e = (u >> f.mbits) & f.exp_mask
+    m = u & ((1 << f.mbits) - 1)
+    normal_sig = (m + (1 << f.mbits)).astype(np.float64)   # 1.m as an integer * 2^mbits
     sub_sig = m.astype(np.float64)
     mag = np.where(
         e == 0,
-        np.ldexp(sub_sig, -133),
-        np.ldexp(normal_sig, (e - 127 - 7).astype(np.int64)),
+        np.ldexp(sub_sig, f.sub_exp),
+        np.ldexp(normal_sig, (e - f.bias - f.mbits).astype(np.int64)),
     )
-    mag = np.where(e == 255, np.where(m == 0, np.inf, np.nan), mag)
+    mag = np.where(e == f.exp_mask, np.where(m == 0, np.inf, np.nan), mag)
     return np.where(sign == 1, -mag, mag)
 
 
-def bf16_encode_rne(x) -> np.ndarray:
-    """float64 values -> BF16 bit patterns, one rounding to nearest even.
+def encode_rne(x, fmt="bf16") -> np.ndarray:
+    """float64 values -> bit patterns of format `fmt`, one rounding to nearest
+    even.
 
     The rounding is done on an integer significand: |x| is scaled by an exact
-    power of two so that one BF16 quantum becomes 1, rounded with np.rint
-    (ties to even), and the bit pattern is assembled from the result.
-    NaN encodes as 0x7FC0 with the input's sign dropped.
+    power of two so that one quantum of the format becomes 1, rounded with
+    np.rint (ties to even), and the bit pattern is assembled from the result.
+    Magnitudes at or above the overflow threshold give infinity; NaN encodes as
+    the format's quiet NaN with the input's sign dropped.
     """
+    f = _fmt(fmt)
     x = np.asarray(x, dtype=np.float64)
     neg = np.signbit(x)
     a = np.abs(x)
@@ -101,38 +137,65 @@ def bf16_encode_rne(x) -> np.ndarray:
     # Unbiased exponent E with |x| = 1.f * 2^E (frexp gives mantissa in [0.5, 1)).
     _, fe = np.frexp(a_safe)
     E = fe.astype(np.int64) - 1
-    # BF16 quantum at this magnitude: 2^(E-7) for normals, 2^-133 below 2^-126.
-    qexp = np.where(a_safe < _BF16_MIN_NORMAL, -133, E - 7)
+    # Quantum at this magnitude: 2^(E - mbits) for normals, 2^sub_exp below
+    # the smallest normal.
+    qexp = np.where(a_safe < f.min_normal, f.sub_exp, E - f.mbits)
     n = np.ldexp(a_safe, -qexp)                           # exact scaling
     r = np.rint(n)                                         # ties to even
     y = np.ldexp(r, qexp)                                  # rounded magnitude, exact
 
-    # Assemble the bits of y (which is exactly a BF16 value or >= 2^128).
+    # Assemble the bits of y (exactly a value of the format, or >= 2^(emax+1)).
     _, ye = np.frexp(y)
     yE = ye.astype(np.int64) - 1
-    is_sub = y < _BF16_MIN_NORMAL
-    sub_bits = np.where(is_sub, np.ldexp(y, 133), 0.0).astype(np.int64)
-    mant = np.where(is_sub, 0, np.ldexp(y, -(yE - 7)).astype(np.int64) - 128)
-    norm_bits = ((yE + 127) << 7) | np.clip(mant, 0, 127)
+    is_sub = y < f.min_normal
+    sub_bits = np.where(is_sub, np.ldexp(y, -f.sub_exp), 0.0).astype(np.int64)
+    mant = np.where(is_sub, 0, np.ldexp(y, -(yE - f.mbits)).astype(np.int64) - (1 << f.mbits))
+    norm_bits = ((yE + f.bias) << f.mbits) | np.clip(mant, 0, (1 << f.mbits) - 1)
     bits = np.where(is_sub, sub_bits, norm_bits)
-    bits = np.where((y >= 2.0 ** 128) | (a >= _BF16_OVERFLOW), 0x7F80, bits)
+    bits = np.where((y >= 2.0 ** (f.emax + 1)) | (a >= f.overflow), f.inf_bits, bits)
     bits = np.where(neg, bits | 0x8000, bits)
-    bits = np.where(nan, int(_BF16_QNAN), bits)
+    bits = np.where(nan, f.qnan_bits, bits)
     return bits.astype(np.uint16)
 
 
-def fold(prefix, add, add2=None):
-    """Step (a2): the MoE-tail fold into the BF16 prefix sum.
+def bf16_decode(bits) -> np.ndarray:
+    """BF16 (1 sign, 8 exponent bits with bias 127, 7 mantissa bits;
+    subnormals mantissa * 2^-133) -> exact float64."""
+    return decode(bits, BF16)
+
+
+def bf16_encode_rne(x) -> np.ndarray:
+    """float64 -> BF16 bits, one rounding to nearest even (NaN -> 0x7FC0)."""
+    return encode_rne(x, BF16)
+
+
+def fp16_decode(bits) -> np.ndarray:
+    """FP16 (IEEE binary16: 1 sign, 5 exponent bits with bias 15, 10 mantissa
+    bits; subnormals mantissa * 2^-24) -> exact float64."""
+    return decode(bits, FP16)
+
+
+def fp16_encode_rne(x) -> np.ndarray:
+    """float64 -> FP16 bits, one rounding to nearest even (|x| >= 65520 gives
+    infinity; NaN -> 0x7E00)."""
+    return encode_rne(x, FP16)
+
+
+def fold(prefix, add, add2=None, fmt="bf16"):
+    """Step (a2): the MoE-tail fold into the prefix sum.
 
     Returns (new_prefix_bits, s_bits) with s = bf16(add + add2) (or add when
     add2 is None) and new_prefix = bf16(prefix + s), each a correctly rounded
-    BF16 addition.  TensorRT-LLM PR #20546, section "Op".
+    BF16 addition.  TensorRT-LLM PR #20546, section "Op".  With fmt="fp16"
+    every tensor and both roundings are FP16 instead (the exact sum of two
+    FP16 values rounded to float64 and then to FP16 is the correctly rounded
+    FP16 sum, 53 >= 2*11+2; the float32 route qualifies too, 24 >= 24).
     """
     if add2 is None:
         s = np.asarray(add, dtype=np.uint16)
     else:
-        s = bf16_encode_rne(bf16_decode(add) + bf16_decode(add2))
-    np_bits = bf16_encode_rne(bf16_decode(prefix) + bf16_decode(s))
+        s = encode_rne(decode(add, fmt) + decode(add2, fmt), fmt)
+    np_bits = encode_rne(decode(prefix, fmt) + decode(s, fmt), fmt)
     return np_bits, s
 
 
@@ -173,8 +236,8 @@ def mixture(V, w, gamma, eps):
 
 
 def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, tokens=None, chunk=64,
-                        with_h=False):
-    """The whole op on BF16 bit patterns.
+                        with_h=False, fmt="bf16"):
+    """The whole op on BF16 bit patterns (FP16 with fmt="fp16").
 
     prefix, add, add2: (M, H) uint16 (add2 may be None);  bank: (N, M, H)
     uint16;  w, gamma: (H,) uint16;  eps: the float32 epsilon the GPU sees
@@ -196,8 +259,8 @@ def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, tokens=None, chu
         tokens = np.arange(M)
     tokens = np.asarray(tokens, dtype=np.int64)
     eps64 = float(np.float32(eps))
-    w64 = bf16_decode(w)
-    g64 = bf16_decode(gamma)
+    w64 = decode(w, fmt)
+    g64 = decode(gamma, fmt)
 
     np_all = np.empty((len(tokens), H), dtype=np.uint16)
     out_all = np.empty((len(tokens), H), dtype=np.float64)
@@ -209,10 +272,11 @@ def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, tokens=None, chu
         if add is None:
             np_bits = prefix[t]          # no fold: the prefix itself is the source
         else:
-            np_bits, _ = fold(prefix[t], add[t], None if add2 is None else np.asarray(add2, dtype=np.uint16)[t])
+            np_bits, _ = fold(prefix[t], add[t],
+                              None if add2 is None else np.asarray(add2, dtype=np.uint16)[t], fmt)
         V = np.empty((len(t), N + 1, H), dtype=np.float64)
-        V[:, :N, :] = bf16_decode(bank[:, t, :]).transpose(1, 0, 2)
-        V[:, N, :] = bf16_decode(np_bits)
+        V[:, :N, :] = decode(bank[:, t, :], fmt).transpose(1, 0, 2)
+        V[:, N, :] = decode(np_bits, fmt)
         r = mixture(V, w64, g64, eps64)
         np_all[c0:c0 + len(t)] = np_bits
         out_all[c0:c0 + len(t)] = r["out"]
@@ -225,14 +289,15 @@ def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, tokens=None, chu
     return np_all, out_all, bound_all
 
 
-def attnres_rmsnorm(prefix, bank, w, gamma, eps, tokens=None, chunk=64, with_h=False):
+def attnres_rmsnorm(prefix, bank, w, gamma, eps, tokens=None, chunk=64, with_h=False,
+                    fmt="bf16"):
     """The attention-residual + RMSNorm alone (no fold): the sources are
     bank[0..N-1, m] and prefix[m] itself.  TensorRT-LLM PR #20546, section
     "Performance", measures the fused epilogue against this op.
 
     Returns (out (T, H) float64, bound (T, H)) [, h, h_bound with with_h]."""
     r = attnres_add_rmsnorm(prefix, None, None, bank, w, gamma, eps, tokens=tokens, chunk=chunk,
-                            with_h=with_h)
+                            with_h=with_h, fmt=fmt)
     return r[1:]
 
 

@@ -1,4 +1,4 @@
-"""Parity criteria between a BF16 GPU result and the float64 oracle.
+"""Parity criteria between a BF16 (or FP16) GPU result and the float64 oracle.
 
 TEST INFRASTRUCTURE ONLY (see oracle/attnres_oracle.py).
 
@@ -19,12 +19,18 @@ float32 accumulation of O(1) terms carries an absolute error near
 the absolute cap for |out| <= 4.  Every element that passes only through the
 floor must still satisfy |delta| <= 64 * 2^-24 * bound_j + 2^-133 (a float32
 error model of the mixture), and the number of such elements is reported.
+
+FP16 outputs (fmt="fp16") take the same criterion with the FP16 unit in the
+last place, ulp_fp16(x) = 2^(floor(log2|x|) - 10) (2^-24 below 2^-14), and the
+smallest FP16 subnormal 2^-24 in place of 2^-133: 2 FP16 ulp is 8x tighter
+than 2 BF16 ulp, the floor and the float32 error model are those of the same
+float32 arithmetic.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from .attnres_oracle import bf16_decode
+from .attnres_oracle import BF16, _fmt, decode
 
 ULP_FACTOR = 2.0
 ABS_FLOOR = 2.0 ** -16
@@ -33,29 +39,36 @@ CAP_RANGE = 4.0
 F32_BOUND_FACTOR = 64 * 2.0 ** -24
 
 
-def ulp_bf16(x) -> np.ndarray:
+def ulp(x, fmt="bf16") -> np.ndarray:
+    """Unit in the last place of the format at the magnitude of x."""
+    f = _fmt(fmt)
     a = np.abs(np.asarray(x, dtype=np.float64))
     _, e = np.frexp(np.where(a == 0, 1.0, a))
-    ulp = np.ldexp(1.0, (e.astype(np.int64) - 1) - 7)
-    return np.where(a < 2.0 ** -126, 2.0 ** -133, ulp)
+    u = np.ldexp(1.0, (e.astype(np.int64) - 1) - f.mbits)
+    return np.where(a < f.min_normal, 2.0 ** f.sub_exp, u)
 
 
-def check_out(gpu_bits, ref, bound):
+def ulp_bf16(x) -> np.ndarray:
+    return ulp(x, BF16)
+
+
+def check_out(gpu_bits, ref, bound, fmt="bf16"):
     """Returns a dict: ok, n, n_fail, n_floor (elements passing only through
     the absolute floor), max_abs, max_ulp, first failing index if any."""
-    got = bf16_decode(gpu_bits)
+    f = _fmt(fmt)
+    got = decode(gpu_bits, f)
     ref = np.asarray(ref, dtype=np.float64)
     bound = np.asarray(bound, dtype=np.float64)
     finite = np.isfinite(ref)
     delta = np.abs(got - ref)
     delta = np.where(finite, delta, 0.0)
-    ulp = ulp_bf16(ref)
-    strict = delta <= ULP_FACTOR * ulp
-    tol = np.maximum(ULP_FACTOR * ulp, ABS_FLOOR)
+    u = ulp(ref, f)
+    strict = delta <= ULP_FACTOR * u
+    tol = np.maximum(ULP_FACTOR * u, ABS_FLOOR)
     ok1 = delta <= tol
     ok2 = (np.abs(ref) > CAP_RANGE) | (delta <= CAP_ABS)
     floor_only = ok1 & ~strict
-    ok3 = ~floor_only | (delta <= F32_BOUND_FACTOR * bound + 2.0 ** -133)
+    ok3 = ~floor_only | (delta <= F32_BOUND_FACTOR * bound + 2.0 ** f.sub_exp)
     okv = (ok1 & ok2 & ok3) | ~finite
     fails = np.flatnonzero(~okv.ravel())
     return {
@@ -64,6 +77,6 @@ def check_out(gpu_bits, ref, bound):
         "n_fail": int(fails.size),
         "n_floor": int(np.count_nonzero(floor_only)),
         "max_abs": float(delta.max()) if delta.size else 0.0,
-        "max_ulp": float((delta / ulp).max()) if delta.size else 0.0,
+        "max_ulp": float((delta / u).max()) if delta.size else 0.0,
         "first_fail": None if fails.size == 0 else np.unravel_index(fails[0], okv.shape),
     }
