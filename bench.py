@@ -411,54 +411,66 @@ def comparators(binding, reps=200):
     return res
 
 
-def deep_banks(binding, wl, peak, steps=5, warmup=3):
-    """Banks deeper than the PR's fused path takes (TensorRT-LLM PR #20546,
-    section "Op": N > 12 falls back there), fused here: GB/s per call at
-    M = 8192 tokens (inputs larger than L2; CUDA events around each call) and
-    warm decode microseconds per call at M = 1 and 32 (CUDA-graph replays),
-    both addends, for N = 16, 24 and 31."""
+def _domain_row(binding, wl, N, dtype, peak, seed, steps=5, warmup=3):
+    """GB/s per call at M = 8192 tokens (inputs larger than L2; CUDA events
+    around each call) and warm decode microseconds per call at M = 1 and 32
+    (CUDA-graph replays), both addends, for N snapshots of `dtype` tensors."""
     import torch
     s = torch.cuda.Stream()
-    res = {}
-    for N in (16, 24, 31):
-        inp = wl.bandwidth_inputs(device="cuda", seed=60 + N, M=M_BW, N=N)
-        out, newp = torch.empty_like(inp.prefix), torch.empty_like(inp.prefix)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    rnd = lambda *sh: torch.randn(sh, generator=g, device="cuda").to(dtype)  # noqa: E731
+    P, A, A2, B = rnd(M_BW, H), rnd(M_BW, H), rnd(M_BW, H), rnd(N, M_BW, H)
+    w = (torch.randn(H, generator=g, device="cuda") / H ** 0.5).to(dtype)
+    gam = (1 + 0.1 * torch.randn(H, generator=g, device="cuda")).to(dtype)
+    out, newp = torch.empty_like(P), torch.empty_like(P)
 
-        def call():
-            binding.attnres_add_rmsnorm(inp.prefix, inp.add, inp.add2, inp.bank, inp.w, inp.gamma,
-                                        inp.eps, out, newp, stream=s, check=False)
-        with torch.cuda.stream(s):
-            for _ in range(warmup):
-                call()
-        torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        with torch.cuda.stream(s):
-            for a, b in ev:
-                a.record(s)
-                call()
-                b.record(s)
-        torch.cuda.synchronize()
-        avg = sum(a.elapsed_time(b) for a, b in ev) / steps / 1e3
-        nb = algorithmic_bytes(M_BW, N, H)
-        row = {"M8192_gbs": round(nb / avg / 1e9, 1), "M8192_us": round(avg * 1e6, 2),
-               "M8192_frac": round(nb / avg / 1e9 / peak, 4),
-               "plan_M8192": binding.attnres_plan(M_BW, N, H)}
-        del inp, out, newp
-        torch.cuda.empty_cache()
-        for M in (1, 32):
-            d = wl.make_inputs(M, N, H, seed=70 + N + M, device="cuda")
-            o, npf = torch.empty_like(d.prefix), torch.empty_like(d.prefix)
-
-            def calls(d=d, o=o, npf=npf, reps=100):
-                for _ in range(reps):
-                    binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps,
-                                                o, npf, stream=s, check=False)
-                return reps
-            row[f"M{M}_warm_us"] = _graph_us(calls, s)
-        res[f"N{N}"] = row
+    def call():
+        binding.attnres_add_rmsnorm(P, A, A2, B, w, gam, 1e-6, out, newp, stream=s, check=False)
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            call()
     torch.cuda.synchronize()
-    return res
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with torch.cuda.stream(s):
+        for a, b in ev:
+            a.record(s)
+            call()
+            b.record(s)
+    torch.cuda.synchronize()
+    avg = sum(a.elapsed_time(b) for a, b in ev) / steps / 1e3
+    nb = algorithmic_bytes(M_BW, N, H)
+    row = {"M8192_gbs": round(nb / avg / 1e9, 1), "M8192_us": round(avg * 1e6, 2),
+           "M8192_frac": round(nb / avg / 1e9 / peak, 4),
+           "plan_M8192": binding.attnres_plan(M_BW, N, H)}
+    del P, A, A2, B, out, newp
+    torch.cuda.empty_cache()
+    for M in (1, 32):
+        d = wl.make_inputs(M, N, H, seed=seed + M, device="cuda", dtype=dtype)
+        o, npf = torch.empty_like(d.prefix), torch.empty_like(d.prefix)
+
+        def calls(d=d, o=o, npf=npf, reps=100):
+            for _ in range(reps):
+                binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps,
+                                            o, npf, stream=s, check=False)
+            return reps
+        row[f"M{M}_warm_us"] = _graph_us(calls, s)
+    torch.cuda.synchronize()
+    return row
+
+
+def deep_banks(binding, wl, peak):
+    """Banks deeper than the PR's fused path takes (TensorRT-LLM PR #20546,
+    section "Op": N > 12 falls back there), fused here: N = 16, 24 and 31."""
+    import torch
+    return {f"N{N}": _domain_row(binding, wl, N, torch.bfloat16, peak, 60 + N) for N in (16, 24, 31)}
+
+
+def fp16_tensors(binding, wl, peak):
+    """The op on FP16 tensors (the PR's fused window is BF16), N = 12."""
+    import torch
+    return {"N12": _domain_row(binding, wl, 12, torch.float16, peak, 90)}
 
 
 def chain_benchmark(binding, wl, layers=25):
@@ -632,12 +644,14 @@ def run_ours(args):
     comp = None
     chain = None
     deep = None
+    fp16 = None
     cpu_base = None
     if rank == 0 and not args.no_decode:
         decode = decode_latencies(binding, wl)
         comp = comparators(binding)
         chain = chain_benchmark(binding, wl)
         deep = deep_banks(binding, wl, peaks()[0])
+        fp16 = fp16_tensors(binding, wl, peaks()[0])
     if rank == 0 and not args.no_cpu_baseline:
         # the oracle on the first tokens of this same workload; the GPU's
         # outputs for those tokens are checked against it on the way
@@ -691,6 +705,7 @@ def run_ours(args):
         "fused_vs_alone_and_tail_add_us": comp,
         "chain_25_layers": chain,
         "deep_banks": deep,
+        "fp16_tensors": fp16,
         "cpu_baseline": cpu_base,
     }
     print(json.dumps(line), flush=True)

@@ -26,7 +26,8 @@
  *      library implements.
  *
  * Conventions shared by every entry point
- *   - Tensors are BF16 stored as 16-bit words, row-major, contiguous, in
+ *   - Tensors are BF16 (FP16 for the _f16 entry point and dtype
+ *     ATTNRES_DTYPE_FP16) stored as 16-bit words, row-major, contiguous, in
  *     device memory of the current CUDA device, each 16-byte aligned.
  *     [M,H] tensors have row stride H; the bank is [N,M,H] (snapshot-major:
  *     snapshot i of token m starts at element (i*M + m)*H).
@@ -68,8 +69,13 @@ typedef enum {
   ATTNRES_ERR_EPS = -5,     /* eps is not finite and > 0                   */
   ATTNRES_ERR_CUDA = -6,    /* a CUDA runtime call failed                  */
   ATTNRES_ERR_DEVICE = -7,  /* the current device is not compute 10.3      */
-  ATTNRES_ERR_CONFIG = -8   /* a forced launch configuration is invalid    */
+  ATTNRES_ERR_CONFIG = -8,  /* a forced launch configuration is invalid    */
+  ATTNRES_ERR_DTYPE = -9    /* unknown element type, or FP16 with N > 12   */
 } attnres_status;
+
+/* Element type of every tensor of a call. */
+#define ATTNRES_DTYPE_BF16 0
+#define ATTNRES_DTYPE_FP16 1
 
 #define ATTNRES_MAX_N 31   /* N = 0 is allowed */
 #define ATTNRES_MAX_H 16384
@@ -181,6 +187,22 @@ int attnres_add_rmsnorm_tap(const void* prefix, const void* add, const void* add
                             int M, int N, int H, attnres_stream_t stream);
 
 /*
+ * attnres_add_rmsnorm_f16 -- attnres_add_rmsnorm on FP16 tensors (every
+ * tensor FP16: 1 sign, 5 exponent, 10 mantissa bits): the same steps with
+ * FP16 in place of BF16, s = fp16(add + add2), new_prefix = fp16(prefix + s)
+ * (float32 additions, round to nearest even, FP16 subnormals kept, overflow
+ * to infinity), out = fp16(h / sqrt(mean(h^2) + eps) * gamma).  The PR's
+ * fused window is BF16 only (section "Model"); this is the same op for a
+ * model kept in FP16.  0 <= N <= 12; N > 12 returns ATTNRES_ERR_DTYPE.
+ * Variants 2 and 3 only (attnres_launch with dtype ATTNRES_DTYPE_FP16 takes
+ * the tap and the attention-residual alone too).
+ */
+int attnres_add_rmsnorm_f16(const void* prefix, const void* add, const void* add2,
+                            const void* bank, const void* w, const void* gamma,
+                            float eps, void* out, void* new_prefix,
+                            int M, int N, int H, attnres_stream_t stream);
+
+/*
  * attnres_rmsnorm -- the attention-residual + RMSNorm alone, without the
  * fold: the sources are bank[0..N-1, m] and prefix[m] itself; writes only
  * out.  This is the op the fused epilogue is measured against (section
@@ -212,14 +234,16 @@ typedef struct {
   float eps;
   void* out;
   void* new_prefix;       /* fold != 0: required                          */
-  void* h_out;            /* optional BF16 mixture tap                     */
+  void* h_out;            /* optional mixture tap                          */
   int M, N, H;
   int fold;               /* 1: fused epilogue; 0: attention-residual alone */
+  int dtype;              /* ATTNRES_DTYPE_BF16 or ATTNRES_DTYPE_FP16       */
 } attnres_args;
 
 /* Any of the calls above (tail_add excepted) with a pinned configuration
- * (cfg may be NULL).  The attention-residual alone (fold = 0) exists for
- * variants 2 and 3 only; other variants return ATTNRES_ERR_CONFIG. */
+ * (cfg may be NULL).  The attention-residual alone (fold = 0) and FP16
+ * tensors exist for variants 2 and 3 only; other variants return
+ * ATTNRES_ERR_CONFIG. */
 int attnres_launch(const attnres_args* args, const attnres_config* cfg,
                    attnres_stream_t stream);
 

@@ -17,8 +17,9 @@ LIB_PATH = os.path.join(PKG, "libattnres.so")
 STATUS = {
     0: "ATTNRES_OK", -1: "ATTNRES_ERR_NULL", -2: "ATTNRES_ERR_SHAPE", -3: "ATTNRES_ERR_ALIGN",
     -4: "ATTNRES_ERR_ALIAS", -5: "ATTNRES_ERR_EPS", -6: "ATTNRES_ERR_CUDA",
-    -7: "ATTNRES_ERR_DEVICE", -8: "ATTNRES_ERR_CONFIG",
+    -7: "ATTNRES_ERR_DEVICE", -8: "ATTNRES_ERR_CONFIG", -9: "ATTNRES_ERR_DTYPE",
 }
+DTYPE_BF16, DTYPE_FP16 = 0, 1
 ATTNRES_DEVICE_WAIT_TIMEOUT = 1
 VARIANTS = {"auto": 0, "cta": 1, "cluster": 2, "stream": 3, "pipe": 4}
 
@@ -27,6 +28,7 @@ EXPORTS = (
     "attnres_add_rmsnorm",
     "attnres_add_rmsnorm_ex",
     "attnres_add_rmsnorm_tap",
+    "attnres_add_rmsnorm_f16",
     "attnres_rmsnorm",
     "attnres_tail_add",
     "attnres_launch",
@@ -59,7 +61,7 @@ class Args(ctypes.Structure):
                 ("bank", ctypes.c_void_p), ("w", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
                 ("eps", ctypes.c_float), ("out", ctypes.c_void_p), ("new_prefix", ctypes.c_void_p),
                 ("h_out", ctypes.c_void_p), ("M", ctypes.c_int), ("N", ctypes.c_int),
-                ("H", ctypes.c_int), ("fold", ctypes.c_int)]
+                ("H", ctypes.c_int), ("fold", ctypes.c_int), ("dtype", ctypes.c_int)]
 
 
 _lib = None
@@ -78,6 +80,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     args = [vp, vp, vp, vp, vp, vp, f, vp, vp, i, i, i, vp]
     lib.attnres_add_rmsnorm.argtypes = args
     lib.attnres_add_rmsnorm.restype = i
+    lib.attnres_add_rmsnorm_f16.argtypes = args
+    lib.attnres_add_rmsnorm_f16.restype = i
     lib.attnres_add_rmsnorm_ex.argtypes = args + [ctypes.POINTER(Config)]
     lib.attnres_add_rmsnorm_ex.restype = i
     lib.attnres_plan.argtypes = [i, i, i, i, ctypes.POINTER(Config)]
@@ -136,10 +140,23 @@ def make_config(variant="auto", cluster=0, threads=0, grid_tokens=0, pdl=0, stag
                   int(prefetch))
 
 
-def _check_tensor(name, t, shape=None):
+def _dtype_code(t) -> int:
+    """ATTNRES_DTYPE_* of a torch tensor (bfloat16 or float16)."""
     import torch
-    if t.dtype != torch.bfloat16:
-        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float16:
+        return DTYPE_FP16
+    raise TypeError(f"tensors must be bfloat16 or float16, got {t.dtype}")
+
+
+def _check_tensor(name, t, shape=None, dtype=None):
+    """dtype: the torch dtype every tensor of the call must have (default
+    bfloat16)."""
+    import torch
+    want = torch.bfloat16 if dtype is None else dtype
+    if t.dtype != want:
+        raise TypeError(f"{name} must be {want}, got {t.dtype}")
     if not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
@@ -153,20 +170,33 @@ def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, out, new_prefix,
     """Launch the fused epilogue on torch CUDA tensors (see include/attnres.h).
 
     prefix, add, add2 (or None), out, new_prefix: [M, H]; bank: [N, M, H];
-    w, gamma: [H]; all bfloat16, contiguous, on the current device.
+    w, gamma: [H]; all bfloat16 (or all float16), contiguous, on the current
+    device.
     stream: a torch.cuda.Stream (default: the current stream).
     config: a Config pinning the launch (default: the library's choice).
     """
     N, M, H = bank.shape
+    dt = prefix.dtype
     if check:
+        _dtype_code(prefix)
         for name, t, shp in (("prefix", prefix, (M, H)), ("add", add, (M, H)),
                              ("bank", bank, (N, M, H)), ("w", w, (H,)), ("gamma", gamma, (H,)),
                              ("out", out, (M, H)), ("new_prefix", new_prefix, (M, H))):
-            _check_tensor(name, t, shp)
+            _check_tensor(name, t, shp, dt)
         if add2 is not None:
-            _check_tensor("add2", add2, (M, H))
+            _check_tensor("add2", add2, (M, H), dt)
     lib = load()
     s = _stream_handle(stream)
+    if _dtype_code(prefix) == DTYPE_FP16:
+        if config is None:
+            st = lib.attnres_add_rmsnorm_f16(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(bank),
+                                             _ptr(w), _ptr(gamma), float(eps), _ptr(out),
+                                             _ptr(new_prefix), M, N, H, s)
+            _check(st)
+        else:
+            launch(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, config=config,
+                   stream=stream)
+        return
     if config is None:
         st = lib.attnres_add_rmsnorm(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(bank), _ptr(w),
                                      _ptr(gamma), float(eps), _ptr(out), _ptr(new_prefix),
@@ -180,9 +210,13 @@ def attnres_add_rmsnorm(prefix, add, add2, bank, w, gamma, eps, out, new_prefix,
 
 def attnres_add_rmsnorm_tap(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, h_out,
                             stream=None):
-    """The fused epilogue that also writes h_out = bf16(h), the pre-norm mixture."""
+    """The fused epilogue that also writes h_out = bf16(h), the pre-norm mixture
+    (fp16(h) for float16 tensors)."""
     N, M, H = bank.shape
-    _check_tensor("h_out", h_out, (M, H))
+    _check_tensor("h_out", h_out, (M, H), prefix.dtype)
+    if _dtype_code(prefix) == DTYPE_FP16:
+        launch(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, h_out=h_out, stream=stream)
+        return
     _check(load().attnres_add_rmsnorm_tap(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(bank),
                                           _ptr(w), _ptr(gamma), float(eps), _ptr(out),
                                           _ptr(new_prefix), _ptr(h_out), M, N, H,
@@ -192,10 +226,11 @@ def attnres_add_rmsnorm_tap(prefix, add, add2, bank, w, gamma, eps, out, new_pre
 def attnres_rmsnorm(prefix, bank, w, gamma, eps, out, stream=None, config: Optional[Config] = None):
     """The attention-residual + RMSNorm alone: sources bank[0..N-1] and prefix."""
     N, M, H = bank.shape
+    _dtype_code(prefix)
     for name, t, shp in (("prefix", prefix, (M, H)), ("bank", bank, (N, M, H)), ("w", w, (H,)),
                          ("gamma", gamma, (H,)), ("out", out, (M, H))):
-        _check_tensor(name, t, shp)
-    if config is None:
+        _check_tensor(name, t, shp, prefix.dtype)
+    if config is None and _dtype_code(prefix) == DTYPE_BF16:
         _check(load().attnres_rmsnorm(_ptr(prefix), _ptr(bank), _ptr(w), _ptr(gamma), float(eps),
                                       _ptr(out), M, N, H, _stream_handle(stream)))
     else:
@@ -215,12 +250,16 @@ def attnres_tail_add(prefix, add, add2, new_prefix, stream=None):
 
 
 def launch(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, h_out=None, M=None, N=None,
-           H=None, fold=True, config: Optional[Config] = None, stream=None):
-    """attnres_launch: any fused call with an optional pinned configuration."""
+           H=None, fold=True, config: Optional[Config] = None, stream=None, dtype=None):
+    """attnres_launch: any fused call with an optional pinned configuration.
+    dtype: DTYPE_BF16 or DTYPE_FP16 (default: that of `prefix`)."""
     if M is None:
         N, M, H = bank.shape
+    if dtype is None:
+        dtype = _dtype_code(prefix)
     a = Args(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(bank), _ptr(w), _ptr(gamma), float(eps),
-             _ptr(out), _ptr(new_prefix), _ptr(h_out), int(M), int(N), int(H), int(bool(fold)))
+             _ptr(out), _ptr(new_prefix), _ptr(h_out), int(M), int(N), int(H), int(bool(fold)),
+             int(dtype))
     _check(load().attnres_launch(ctypes.byref(a), None if config is None else ctypes.byref(config),
                                  _stream_handle(stream)))
 

@@ -19,6 +19,8 @@ ATTNRES_UNIT_E(extern)
 ATTNRES_UNIT_F(extern)
 ATTNRES_UNIT_G(extern)
 ATTNRES_UNIT_H(extern)
+ATTNRES_UNIT_I(extern)
+ATTNRES_UNIT_J(extern)
 
 namespace {
 
@@ -104,6 +106,7 @@ struct Args {
   void* h_out;
   int M, N, H;
   bool fold;
+  int dtype;  // ATTNRES_DTYPE_*
 };
 
 int validate_shape(int M, int N, int H) {
@@ -113,10 +116,12 @@ int validate_shape(int M, int N, int H) {
 }
 
 int validate(const Args& a) {
+  if (a.dtype != ATTNRES_DTYPE_BF16 && a.dtype != ATTNRES_DTYPE_FP16) return ATTNRES_ERR_DTYPE;
   if (!a.prefix || (a.N > 0 && !a.bank) || !a.w || !a.gamma || !a.out) return ATTNRES_ERR_NULL;
   if (a.fold && (!a.add || !a.new_prefix)) return ATTNRES_ERR_NULL;
   int st = validate_shape(a.M, a.N, a.H);
   if (st != ATTNRES_OK) return st;
+  if (a.dtype == ATTNRES_DTYPE_FP16 && a.N > kShallowMaxN) return ATTNRES_ERR_DTYPE;
   if (!(a.eps > 0.f) || !isfinite(a.eps)) return ATTNRES_ERR_EPS;
   const void* add = a.fold ? a.add : nullptr;
   const void* add2 = a.fold ? a.add2 : nullptr;
@@ -323,6 +328,27 @@ cudaError_t dispatch_pipe_stages(int stages, const Params& p, dim3 g, int t, int
   }
 }
 
+// FP16 tensors (N <= 12): the split or the streaming shape.
+template <int VPT, int MAXT, int MINB>
+cudaError_t dispatch_fp16(int N, int mode, const Params& p, dim3 g, int t, int c, bool pdl,
+                          cudaStream_t s) {
+#define ATTNRES_CASE(n)                                                                    \
+  case n:                                                                                  \
+    return mode == kFoldAdd2                                                               \
+               ? launch_fused<n, kFoldAdd2, VPT, MAXT, MINB, kFP16>(p, g, t, c, pdl, s)    \
+           : mode == kFoldAdd ? launch_fused<n, kFoldAdd, VPT, MAXT, MINB, kFP16>(p, g, t, c, pdl, s) \
+                              : launch_fused<n, kNoFold, VPT, MAXT, MINB, kFP16>(p, g, t, c, pdl, s);
+  switch (N) {
+    ATTNRES_CASE(0)
+    ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
+    ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
+    ATTNRES_CASE(9) ATTNRES_CASE(10) ATTNRES_CASE(11) ATTNRES_CASE(12)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef ATTNRES_CASE
+}
+
 // Deep banks: the split shape (STREAM false) or the deep streaming shape,
 // with or without the fold.
 template <int N, bool STREAM>
@@ -379,8 +405,10 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   const bool has_add2 = a.fold && a.add2 != nullptr;
   attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0, 0, 0};
   if ((st = resolve(a.M, a.N, has_add2, a.H, sms, &c)) != ATTNRES_OK) return st;
-  // the attention-residual alone exists in the two fused shapes only
-  if (!a.fold && c.variant != 2 && c.variant != 3) return ATTNRES_ERR_CONFIG;
+  // the attention-residual alone and FP16 tensors exist in the two fused
+  // shapes only
+  if ((!a.fold || a.dtype == ATTNRES_DTYPE_FP16) && c.variant != 2 && c.variant != 3)
+    return ATTNRES_ERR_CONFIG;
 
   Params p;
   p.prefix = static_cast<const uint4*>(a.prefix);
@@ -407,7 +435,13 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   const bool pdl = c.pdl >= 0;
   cudaError_t e;
   const int mode = !a.fold ? kNoFold : has_add2 ? kFoldAdd2 : kFoldAdd;
-  if (a.N > kShallowMaxN && c.variant == 2)
+  if (a.dtype == ATTNRES_DTYPE_FP16 && c.variant == 2)
+    e = dispatch_fp16<kSplitVPT, kSplitMaxT, kSplitMinB>(a.N, mode, p, grid, c.threads, c.cluster,
+                                                         pdl, s);
+  else if (a.dtype == ATTNRES_DTYPE_FP16)
+    e = dispatch_fp16<kStreamVPT, kStreamMaxT, kStreamMinB>(a.N, mode, p, grid, c.threads,
+                                                            c.cluster, pdl, s);
+  else if (a.N > kShallowMaxN && c.variant == 2)
     e = dispatch_deep<false>(a.N, mode, p, grid, c.threads, c.cluster, pdl, s);
   else if (a.N > kShallowMaxN)
     e = dispatch_deep<true>(a.N, mode, p, grid, c.threads, c.cluster, pdl, s);
@@ -432,7 +466,7 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
 
 Args make_args(const void* prefix, const void* add, const void* add2, const void* bank,
                const void* w, const void* gamma, float eps, void* out, void* new_prefix,
-               void* h_out, int M, int N, int H, bool fold) {
+               void* h_out, int M, int N, int H, bool fold, int dtype = ATTNRES_DTYPE_BF16) {
   Args a;
   a.prefix = prefix;
   a.add = add;
@@ -448,6 +482,7 @@ Args make_args(const void* prefix, const void* add, const void* add2, const void
   a.N = N;
   a.H = H;
   a.fold = fold;
+  a.dtype = dtype;
   return a;
 }
 
@@ -474,6 +509,15 @@ extern "C" int attnres_add_rmsnorm(const void* prefix, const void* add, const vo
                                 stream, nullptr);
 }
 
+extern "C" int attnres_add_rmsnorm_f16(const void* prefix, const void* add, const void* add2,
+                                       const void* bank, const void* w, const void* gamma,
+                                       float eps, void* out, void* new_prefix, int M, int N, int H,
+                                       attnres_stream_t stream) {
+  return run(make_args(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, nullptr, M, N, H,
+                       true, ATTNRES_DTYPE_FP16),
+             nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" int attnres_add_rmsnorm_tap(const void* prefix, const void* add, const void* add2,
                                        const void* bank, const void* w, const void* gamma,
                                        float eps, void* out, void* new_prefix, void* h_out, int M,
@@ -497,7 +541,7 @@ extern "C" int attnres_launch(const attnres_args* args, const attnres_config* cf
   if (!args) return ATTNRES_ERR_NULL;
   return run(make_args(args->prefix, args->add, args->add2, args->bank, args->w, args->gamma,
                        args->eps, args->out, args->new_prefix, args->h_out, args->M, args->N,
-                       args->H, args->fold != 0),
+                       args->H, args->fold != 0, args->dtype),
              cfg, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -549,6 +593,7 @@ extern "C" const char* attnres_status_string(int status) {
     case ATTNRES_ERR_CUDA: return "a CUDA runtime call failed (see attnres_last_cuda_error)";
     case ATTNRES_ERR_DEVICE: return "the current device is not a compute capability 10.3 GPU";
     case ATTNRES_ERR_CONFIG: return "invalid launch configuration";
+    case ATTNRES_ERR_DTYPE: return "unsupported element type: BF16, or FP16 with N <= 12";
     default: return "unknown status";
   }
 }

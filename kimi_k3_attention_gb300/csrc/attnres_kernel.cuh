@@ -125,52 +125,90 @@ __device__ __forceinline__ float mul_rn(float a, float b) {
   return r;
 }
 
-// Two float32 -> packed BF16x2, each rounded to nearest even (no .ftz form
-// exists for this conversion; subnormal results are kept).  `lo` lands in
-// the low 16 bits.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
+// Element formats of the tensors: BF16 (the model's) and FP16.  For each,
+// the 16-bit halves of a 32-bit word unpacked to exact float32 (`lo` is the
+// low half), two float32 packed into one word with one rounding to nearest
+// even each (no .ftz: subnormal results are kept), and the per-source sums
+// of a word's two lanes: ss += x*x, d += w*x, each a float32 FMA rounded
+// once.  The products of two BF16 or two FP16 values are exact in float32,
+// so the mixed-precision FMA (16-bit operands, float32 accumulator) gives
+// the same bits as unpacking both operands and using fma.rn.f32, without
+// the unpacking instructions.
+constexpr int kBF16 = 0, kFP16 = 1;
 
-// BF16 halves of a 32-bit word -> exact float32 (integer moves only).
-__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+template <int DT>
+struct Fmt;
 
+template <>
+struct Fmt<kBF16> {
+  // integer moves only
+  static __device__ __forceinline__ float lo(uint32_t u) { return __uint_as_float(u << 16); }
+  static __device__ __forceinline__ float hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  }
+  static __device__ __forceinline__ void stats(uint32_t x, uint32_t w, float& ss, float& d) {
+    asm("{\n .reg .b16 xl, xh, wl, wh;\n mov.b32 {xl, xh}, %2;\n mov.b32 {wl, wh}, %3;\n"
+        " fma.rn.f32.bf16 %0, xl, xl, %0;\n fma.rn.f32.bf16 %1, wl, xl, %1;\n"
+        " fma.rn.f32.bf16 %0, xh, xh, %0;\n fma.rn.f32.bf16 %1, wh, xh, %1;\n}"
+        : "+f"(ss), "+f"(d)
+        : "r"(x), "r"(w));
+  }
+};
+
+template <>
+struct Fmt<kFP16> {
+  // FP16 subnormals are normal float32 values: the conversion is exact
+  static __device__ __forceinline__ float lo(uint32_t u) {
+    float r;
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, l;\n}" : "=f"(r) : "r"(u));
+    return r;
+  }
+  static __device__ __forceinline__ float hi(uint32_t u) {
+    float r;
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(r) : "r"(u));
+    return r;
+  }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  }
+  static __device__ __forceinline__ void stats(uint32_t x, uint32_t w, float& ss, float& d) {
+    asm("{\n .reg .b16 xl, xh, wl, wh;\n mov.b32 {xl, xh}, %2;\n mov.b32 {wl, wh}, %3;\n"
+        " fma.rn.f32.f16 %0, xl, xl, %0;\n fma.rn.f32.f16 %1, wl, xl, %1;\n"
+        " fma.rn.f32.f16 %0, xh, xh, %0;\n fma.rn.f32.f16 %1, wh, xh, %1;\n}"
+        : "+f"(ss), "+f"(d)
+        : "r"(x), "r"(w));
+  }
+};
+
+// Element e (0..7) of a 16-byte chunk as float32.
+template <int DT>
 __device__ __forceinline__ float elem(const uint4& v, int e) {
   const uint32_t u = (e < 2) ? v.x : (e < 4) ? v.y : (e < 6) ? v.z : v.w;
-  return (e & 1) ? bf_hi(u) : bf_lo(u);
+  return (e & 1) ? Fmt<DT>::hi(u) : Fmt<DT>::lo(u);
 }
 
-// Sums of squares and of products with w for the two BF16 lanes of a word,
-// low lane first: ss += x*x, d += w*x, each a float32 FMA rounded once.  The
-// products of two BF16 values are exact in float32, so the mixed-precision
-// form (BF16 operands, float32 accumulator) gives the same bits as unpacking
-// both operands and using fma.rn.f32, without the unpacking instructions.
-__device__ __forceinline__ void stats_word(uint32_t x, uint32_t w, float& ss, float& d) {
-  asm("{\n .reg .b16 xl, xh, wl, wh;\n mov.b32 {xl, xh}, %2;\n mov.b32 {wl, wh}, %3;\n"
-      " fma.rn.f32.bf16 %0, xl, xl, %0;\n fma.rn.f32.bf16 %1, wl, xl, %1;\n"
-      " fma.rn.f32.bf16 %0, xh, xh, %0;\n fma.rn.f32.bf16 %1, wh, xh, %1;\n}"
-      : "+f"(ss), "+f"(d)
-      : "r"(x), "r"(w));
-}
-
-// One 32-bit word (two BF16 lanes) of the fold.
-template <bool ADD2>
+// One 32-bit word (two lanes) of the fold: float32 additions, each result
+// rounded to the element format.
+template <bool ADD2, int DT>
 __device__ __forceinline__ uint32_t fold_word(uint32_t p, uint32_t a, uint32_t a2) {
+  using F = Fmt<DT>;
   uint32_t s = a;
-  if (ADD2) s = pack_bf16x2(add_rn(bf_lo(a), bf_lo(a2)), add_rn(bf_hi(a), bf_hi(a2)));
-  return pack_bf16x2(add_rn(bf_lo(p), bf_lo(s)), add_rn(bf_hi(p), bf_hi(s)));
+  if (ADD2) s = F::pack(add_rn(F::lo(a), F::lo(a2)), add_rn(F::hi(a), F::hi(a2)));
+  return F::pack(add_rn(F::lo(p), F::lo(s)), add_rn(F::hi(p), F::hi(s)));
 }
 
-template <bool ADD2>
+template <bool ADD2, int DT>
 __device__ __forceinline__ uint4 fold_chunk(const uint4& p, const uint4& a, const uint4& a2) {
   uint4 r;
-  r.x = fold_word<ADD2>(p.x, a.x, a2.x);
-  r.y = fold_word<ADD2>(p.y, a.y, a2.y);
-  r.z = fold_word<ADD2>(p.z, a.z, a2.z);
-  r.w = fold_word<ADD2>(p.w, a.w, a2.w);
+  r.x = fold_word<ADD2, DT>(p.x, a.x, a2.x);
+  r.y = fold_word<ADD2, DT>(p.y, a.y, a2.y);
+  r.z = fold_word<ADD2, DT>(p.z, a.z, a2.z);
+  r.w = fold_word<ADD2, DT>(p.w, a.w, a2.w);
   return r;
 }
 
@@ -493,7 +531,7 @@ struct SmemSources {
 // Sums of squares and dot products with w of sources I0..I1-1 over this
 // thread's chunks: part[2(i - I0)] = ss_i, part[2(i - I0) + 1] = d_i, the
 // rest of the KP slots zero.
-template <int I0, int I1, int KP, int VPT, class Src>
+template <int I0, int I1, int KP, int VPT, int DT, class Src>
 __device__ __forceinline__ void source_sums(const Src& src, const uint4 (&wv)[VPT],
                                             float (&part)[KP]) {
 #pragma unroll
@@ -502,10 +540,10 @@ __device__ __forceinline__ void source_sums(const Src& src, const uint4 (&wv)[VP
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const uint4 u = src.get(i, k);
-      stats_word(u.x, wv[k].x, ss, d);
-      stats_word(u.y, wv[k].y, ss, d);
-      stats_word(u.z, wv[k].z, ss, d);
-      stats_word(u.w, wv[k].w, ss, d);
+      Fmt<DT>::stats(u.x, wv[k].x, ss, d);
+      Fmt<DT>::stats(u.y, wv[k].y, ss, d);
+      Fmt<DT>::stats(u.z, wv[k].z, ss, d);
+      Fmt<DT>::stats(u.w, wv[k].w, ss, d);
     }
     part[2 * (i - I0)] = ss;
     part[2 * (i - I0) + 1] = d;
@@ -519,7 +557,7 @@ __device__ __forceinline__ void source_sums(const Src& src, const uint4 (&wv)[VP
 // addend chunks, src gives the bank chunks (and receives the updated prefix),
 // wv the pseudo-query chunks; masked chunks (ok false) are zeros and store
 // nothing.
-template <int N, int MODE, int VPT, class Src>
+template <int N, int MODE, int VPT, int DT, class Src>
 __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>::G>& x, Thread& t,
                                                size_t row, const int (&jj)[VPT],
                                                const bool (&ok)[VPT], const uint4 (&wv)[VPT],
@@ -535,21 +573,21 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
   // flight would make the release barriers below wait for it)
 #pragma unroll
   for (int k = 0; k < VPT; ++k)
-    src.set_new_prefix(k, MODE == kNoFold ? pr[k] : fold_chunk<MODE == kFoldAdd2>(pr[k], ad[k], ad2[k]));
+    src.set_new_prefix(k, MODE == kNoFold ? pr[k] : fold_chunk<MODE == kFoldAdd2, DT>(pr[k], ad[k], ad2[k]));
 
   // ---- per-source sums of squares and dot products with w, and R1: warp
   // transpose-reduction per group, CTA sum, st.async to every CTA
   float wt0, wt1 = 0.f;
   {
     float part0[SL::KP0];
-    source_sums<0, S0>(src, wv, part0);
+    source_sums<0, S0, SL::KP0, VPT, DT>(src, wv, part0);
     if constexpr (SL::G == 1) {
       src.fence();
       wt0 = warp_transpose_reduce<SL::KP0>(part0, lane);
     } else {
       wt0 = warp_transpose_reduce<SL::KP0>(part0, lane);
       float part1[SL::KP1 > 0 ? SL::KP1 : 1];
-      source_sums<16, S>(src, wv, part1);
+      source_sums<16, S, (SL::KP1 > 0 ? SL::KP1 : 1), VPT, DT>(src, wv, part1);
       src.fence();
       wt1 = warp_transpose_reduce<SL::KP1>(part1, lane);
     }
@@ -624,13 +662,13 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
     {
       const uint4 u = src.get(0, k);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) h[k][e] = mul_rn(alpha[0], elem(u, e));
+      for (int e = 0; e < 8; ++e) h[k][e] = mul_rn(alpha[0], elem<DT>(u, e));
     }
 #pragma unroll
     for (int i = 1; i < S; ++i) {
       const uint4 u = src.get(i, k);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) h[k][e] = fma_rn(alpha[i], elem(u, e), h[k][e]);
+      for (int e = 0; e < 8; ++e) h[k][e] = fma_rn(alpha[i], elem<DT>(u, e), h[k][e]);
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) q = fma_rn(h[k][e], h[k][e], q);
@@ -658,21 +696,21 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
       if (MODE != kNoFold) st_out(p.new_prefix + row + jj[k], src.new_prefix(k));
       if (p.h_out != nullptr) {
         uint4 hv;
-        hv.x = pack_bf16x2(h[k][0], h[k][1]);
-        hv.y = pack_bf16x2(h[k][2], h[k][3]);
-        hv.z = pack_bf16x2(h[k][4], h[k][5]);
-        hv.w = pack_bf16x2(h[k][6], h[k][7]);
+        hv.x = Fmt<DT>::pack(h[k][0], h[k][1]);
+        hv.y = Fmt<DT>::pack(h[k][2], h[k][3]);
+        hv.z = Fmt<DT>::pack(h[k][4], h[k][5]);
+        hv.w = Fmt<DT>::pack(h[k][6], h[k][7]);
         st_out(p.h_out + row + jj[k], hv);
       }
       uint4 o;
-      o.x = pack_bf16x2(mul_rn(mul_rn(h[k][0], rh), elem(gv[k], 0)),
-                        mul_rn(mul_rn(h[k][1], rh), elem(gv[k], 1)));
-      o.y = pack_bf16x2(mul_rn(mul_rn(h[k][2], rh), elem(gv[k], 2)),
-                        mul_rn(mul_rn(h[k][3], rh), elem(gv[k], 3)));
-      o.z = pack_bf16x2(mul_rn(mul_rn(h[k][4], rh), elem(gv[k], 4)),
-                        mul_rn(mul_rn(h[k][5], rh), elem(gv[k], 5)));
-      o.w = pack_bf16x2(mul_rn(mul_rn(h[k][6], rh), elem(gv[k], 6)),
-                        mul_rn(mul_rn(h[k][7], rh), elem(gv[k], 7)));
+      o.x = Fmt<DT>::pack(mul_rn(mul_rn(h[k][0], rh), elem<DT>(gv[k], 0)),
+                          mul_rn(mul_rn(h[k][1], rh), elem<DT>(gv[k], 1)));
+      o.y = Fmt<DT>::pack(mul_rn(mul_rn(h[k][2], rh), elem<DT>(gv[k], 2)),
+                          mul_rn(mul_rn(h[k][3], rh), elem<DT>(gv[k], 3)));
+      o.z = Fmt<DT>::pack(mul_rn(mul_rn(h[k][4], rh), elem<DT>(gv[k], 4)),
+                          mul_rn(mul_rn(h[k][5], rh), elem<DT>(gv[k], 5)));
+      o.w = Fmt<DT>::pack(mul_rn(mul_rn(h[k][6], rh), elem<DT>(gv[k], 6)),
+                          mul_rn(mul_rn(h[k][7], rh), elem<DT>(gv[k], 7)));
       st_out(p.out + row + jj[k], o);
     }
   }
@@ -694,8 +732,8 @@ __device__ __forceinline__ Thread thread_info() {
 // ---------------------------------------------------------------- kernels
 
 // Loads straight to registers; each cluster handles tokens blockIdx.y,
-// blockIdx.y + gridDim.y, ...
-template <int N, int MODE, int VPT, int MAXT, int MINB>
+// blockIdx.y + gridDim.y, ...  DT is the element format of every tensor.
+template <int N, int MODE, int VPT, int MAXT, int MINB, int DT = kBF16>
 __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params p) {
   __shared__ Exchange<Sums<N>::G> x;
   Thread t = thread_info();
@@ -781,7 +819,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     griddep_launch_dependents();
     if (!early_init && m == static_cast<int>(blockIdx.y)) exchange_init<Sums<N>::total>(x, t, p);
     RegSources<N, VPT> src{v};
-    token_epilogue<N, MODE, VPT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
+    token_epilogue<N, MODE, VPT, DT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
   }
   exchange_exit(t, p);
 }
@@ -857,7 +895,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
       a += row_step;
     }
     SmemSources<N> src{a, row_step, ok[0], z};
-    token_epilogue<N, ADD2 ? kFoldAdd2 : kFoldAdd, 1>(p, x, t, static_cast<size_t>(m) * p.H8, jj,
+    token_epilogue<N, ADD2 ? kFoldAdd2 : kFoldAdd, 1, kBF16>(p, x, t, static_cast<size_t>(m) * p.H8, jj,
                                                      ok, wv, gv, pr, ad, ad2, src, first);
     stage = (stage + 1 == STAGES) ? 0 : stage + 1;
   }
@@ -880,13 +918,13 @@ __global__ void __launch_bounds__(256) attnres_tail_add_kernel(const uint4* __re
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += stride) {
     const uint4 a2 = ADD2 ? ld_stream(add2 + i) : make_uint4(0, 0, 0, 0);
-    st_out(new_prefix + i, fold_chunk<ADD2>(ld_stream(prefix + i), ld_stream(add + i), a2));
+    st_out(new_prefix + i, fold_chunk<ADD2, kBF16>(ld_stream(prefix + i), ld_stream(add + i), a2));
   }
   griddep_launch_dependents();
 }
 
 // Host-side launchers of one instantiation (defined in attnres_launch.cuh).
-template <int N, int MODE, int VPT, int MAXT, int MINB>
+template <int N, int MODE, int VPT, int MAXT, int MINB, int DT = kBF16>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
                          cudaStream_t s);
 template <int N, bool ADD2, int STAGES>

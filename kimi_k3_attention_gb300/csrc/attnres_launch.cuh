@@ -28,10 +28,10 @@ constexpr int kShallowMaxN = 12;
 constexpr int kDeepStreamMaxT = 128;
 constexpr int deep_minb(int n) { return n <= 16 ? 5 : n <= 24 ? 4 : 3; }
 
-template <int N, int MODE, int VPT, int MAXT, int MINB>
+template <int N, int MODE, int VPT, int MAXT, int MINB, int DT>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
                          cudaStream_t s) {
-  auto kern = attnres_fused_kernel<N, MODE, VPT, MAXT, MINB>;
+  auto kern = attnres_fused_kernel<N, MODE, VPT, MAXT, MINB, DT>;
   // Cluster sizes above 8 need an opt-in per function and device.
   static std::atomic<unsigned char> opted[kMaxDevices];
   if (cluster > 8) {
@@ -163,6 +163,10 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   DEF template cudaError_t launch_fused<N, MODE, VPT, MAXT, MINB>(const Params&, dim3, int, \
                                                                   int, bool, cudaStream_t);
 
+#define ATTNRES_FUSED_DT(DEF, N, MODE, VPT, MAXT, MINB, DT)                                \
+  DEF template cudaError_t launch_fused<N, MODE, VPT, MAXT, MINB, DT>(const Params&, dim3, int, \
+                                                                      int, bool, cudaStream_t);
+
 #define ATTNRES_PIPE(DEF, N, ADD2, STAGES)                                          \
   DEF template cudaError_t launch_pipe<N, ADD2, STAGES>(const Params&, dim3, int, int, bool, \
                                                         cudaStream_t);
@@ -191,6 +195,16 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   ATTNRES_FUSED(DEF, N, kFoldAdd2, kStreamVPT, kDeepStreamMaxT, deep_minb(N))      \
   ATTNRES_FUSED(DEF, N, kFoldAdd, kStreamVPT, kDeepStreamMaxT, deep_minb(N))       \
   ATTNRES_FUSED(DEF, N, kNoFold, kStreamVPT, kDeepStreamMaxT, deep_minb(N))
+
+// FP16 tensors, N <= 12: the split and streaming shapes, with the fold
+// (add2 present or not) and without.
+#define ATTNRES_INSTANTIATE_FP16(DEF, N)                                               \
+  ATTNRES_FUSED_DT(DEF, N, kFoldAdd2, kSplitVPT, kSplitMaxT, kSplitMinB, kFP16)        \
+  ATTNRES_FUSED_DT(DEF, N, kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB, kFP16)         \
+  ATTNRES_FUSED_DT(DEF, N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB, kFP16)          \
+  ATTNRES_FUSED_DT(DEF, N, kFoldAdd2, kStreamVPT, kStreamMaxT, kStreamMinB, kFP16)     \
+  ATTNRES_FUSED_DT(DEF, N, kFoldAdd, kStreamVPT, kStreamMaxT, kStreamMinB, kFP16)      \
+  ATTNRES_FUSED_DT(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, kStreamMinB, kFP16)
 
 #define ATTNRES_INSTANTIATE_TAIL_ADD(DEF)                                                  \
   DEF template cudaError_t launch_tail_add<true>(const uint4*, const uint4*, const uint4*,  \
@@ -237,5 +251,14 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   ATTNRES_INSTANTIATE_DEEP(DEF, 27) ATTNRES_INSTANTIATE_DEEP(DEF, 28)                   \
   ATTNRES_INSTANTIATE_DEEP(DEF, 29) ATTNRES_INSTANTIATE_DEEP(DEF, 30)                   \
   ATTNRES_INSTANTIATE_DEEP(DEF, 31)
+#define ATTNRES_UNIT_I(DEF)                                                             \
+  ATTNRES_INSTANTIATE_FP16(DEF, 0) ATTNRES_INSTANTIATE_FP16(DEF, 1)                     \
+  ATTNRES_INSTANTIATE_FP16(DEF, 2) ATTNRES_INSTANTIATE_FP16(DEF, 3)                     \
+  ATTNRES_INSTANTIATE_FP16(DEF, 4) ATTNRES_INSTANTIATE_FP16(DEF, 5)                     \
+  ATTNRES_INSTANTIATE_FP16(DEF, 6)
+#define ATTNRES_UNIT_J(DEF)                                                             \
+  ATTNRES_INSTANTIATE_FP16(DEF, 7) ATTNRES_INSTANTIATE_FP16(DEF, 8)                     \
+  ATTNRES_INSTANTIATE_FP16(DEF, 9) ATTNRES_INSTANTIATE_FP16(DEF, 10)                    \
+  ATTNRES_INSTANTIATE_FP16(DEF, 11) ATTNRES_INSTANTIATE_FP16(DEF, 12)
 
 }  // namespace attnres

@@ -2,7 +2,8 @@
 
 This module only draws random tensors; it holds none of the op's arithmetic,
 so both the CUDA path and the CPU oracle can be fed from it.  Every tensor is
-drawn in float32 from a seeded torch.Generator and rounded to BF16 by torch.
+drawn in float32 from a seeded torch.Generator and rounded to BF16 (or, for
+the FP16 workloads, FP16) by torch.
 
 Distributions (the second parameter of N(0, x) is a variance):
   prefix, add, add2, bank ~ N(0, 1);  w ~ N(0, 1/H);  gamma = 1 + 0.1 N(0, 1)
@@ -57,19 +58,21 @@ def _gen(seed: int, device="cpu") -> torch.Generator:
     return g
 
 
-def _normal(shape, std, g, device="cpu"):
-    return (torch.randn(shape, generator=g, dtype=torch.float32, device=device) * std).to(torch.bfloat16)
+def _normal(shape, std, g, device="cpu", dtype=torch.bfloat16):
+    return (torch.randn(shape, generator=g, dtype=torch.float32, device=device) * std).to(dtype)
 
 
-def make_inputs(M, N, H=H_MODEL, seed=0, add2=True, device="cpu", eps=EPS) -> Inputs:
-    """Standard N(0,1) workload.  Draw order: prefix, add, add2, bank, w, gamma."""
+def make_inputs(M, N, H=H_MODEL, seed=0, add2=True, device="cpu", eps=EPS,
+                dtype=torch.bfloat16) -> Inputs:
+    """Standard N(0,1) workload.  Draw order: prefix, add, add2, bank, w, gamma.
+    dtype: torch.bfloat16 (the model's) or torch.float16."""
     g = _gen(seed, device)
-    prefix = _normal((M, H), 1.0, g, device)
-    add = _normal((M, H), 1.0, g, device)
-    a2 = _normal((M, H), 1.0, g, device) if add2 else None
-    bank = _normal((N, M, H), 1.0, g, device)
-    w = _normal((H,), 1.0 / math.sqrt(H), g, device)
-    gamma = (1.0 + 0.1 * torch.randn((H,), generator=g, dtype=torch.float32, device=device)).to(torch.bfloat16)
+    prefix = _normal((M, H), 1.0, g, device, dtype)
+    add = _normal((M, H), 1.0, g, device, dtype)
+    a2 = _normal((M, H), 1.0, g, device, dtype) if add2 else None
+    bank = _normal((N, M, H), 1.0, g, device, dtype)
+    w = _normal((H,), 1.0 / math.sqrt(H), g, device, dtype)
+    gamma = (1.0 + 0.1 * torch.randn((H,), generator=g, dtype=torch.float32, device=device)).to(dtype)
     return Inputs(prefix, add, a2, bank, w, gamma, eps)
 
 

@@ -16,12 +16,13 @@ def u16(t: torch.Tensor) -> np.ndarray:
 
 
 class Guarded:
-    """A [M, H] BF16 device tensor with canary bands before and after it."""
+    """A [M, H] BF16 (or FP16) device tensor with canary bands before and
+    after it."""
 
-    def __init__(self, shape, device="cuda"):
+    def __init__(self, shape, device="cuda", dtype=torch.bfloat16):
         n = int(np.prod(shape))
         self.buf = torch.full((GUARD + n + GUARD,), CANARY, dtype=torch.int16, device=device)
-        self.t = self.buf[GUARD:GUARD + n].view(torch.bfloat16).view(*shape)
+        self.t = self.buf[GUARD:GUARD + n].view(dtype).view(*shape)
 
     def guards_intact(self) -> bool:
         b = self.buf.cpu()
@@ -32,8 +33,8 @@ def run_gpu(inp, config=None, stream=None):
     """Run the op through the C ABI on device copies of `inp` (an Inputs on
     the CPU or the GPU).  Returns (new_prefix_bits, out_bits) as numpy."""
     d = inp.to("cuda")
-    out = Guarded((inp.M, inp.H))
-    newp = Guarded((inp.M, inp.H))
+    out = Guarded((inp.M, inp.H), dtype=inp.prefix.dtype)
+    newp = Guarded((inp.M, inp.H), dtype=inp.prefix.dtype)
     binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps,
                                 out.t, newp.t, stream=stream, config=config)
     torch.cuda.synchronize()
@@ -43,9 +44,15 @@ def run_gpu(inp, config=None, stream=None):
     return u16(newp.t), u16(out.t)
 
 
+def fmt_of(inp) -> str:
+    """The oracle's name of the element format of an Inputs."""
+    return "fp16" if inp.prefix.dtype == torch.float16 else "bf16"
+
+
 def oracle(inp, tokens=None):
     return oracle_op(u16(inp.prefix), u16(inp.add), None if inp.add2 is None else u16(inp.add2),
-                     u16(inp.bank), u16(inp.w), u16(inp.gamma), inp.eps, tokens=tokens)
+                     u16(inp.bank), u16(inp.w), u16(inp.gamma), inp.eps, tokens=tokens,
+                     fmt=fmt_of(inp))
 
 
 def assert_parity(inp, gpu_np, gpu_out, tokens=None, label=""):
@@ -55,7 +62,7 @@ def assert_parity(inp, gpu_np, gpu_out, tokens=None, label=""):
     bad = np.flatnonzero((gpu_np != ref_np).ravel())
     assert bad.size == 0, (f"{label}: new_prefix differs at {bad.size} elements, first flat index "
                            f"{bad[0]}: gpu {gpu_np.ravel()[bad[0]]:#06x} oracle {ref_np.ravel()[bad[0]]:#06x}")
-    r = check_out(gpu_out, ref_out, bound)
+    r = check_out(gpu_out, ref_out, bound, fmt_of(inp))
     assert r["ok"], f"{label}: out outside tolerance: {r}"
     return r
 

@@ -128,7 +128,51 @@ def test_new_entry_points_validate_on_host():
     assert lib.attnres_launch(None, None, None) == -1
 
 
-def test_args_struct_layout():
-    # 6 pointers, eps (+4 bytes of padding), 3 pointers, 4 ints: the C layout
-    assert ctypes.sizeof(binding.Args) == 6 * 8 + 8 + 3 * 8 + 4 * 4 == 96
-    assert binding.Args.out.offset == 56 and binding.Args.M.offset == 80
+def _c_layout():
+    """sizeof / offsetof of the header's structs, from a C program compiled
+    against include/attnres.h."""
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = {"attnres_args": [f for f, _ in binding.Args._fields_],
+              "attnres_config": [f for f, _ in binding.Config._fields_]}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "attnres.h"', "int main(void) {"]
+    for st, fs in fields.items():
+        lines.append(f'  printf("{st} sizeof %zu\\n", sizeof({st}));')
+        for f in fs:
+            lines.append(f'  printf("{st} {f} %zu\\n", offsetof({st}, {f}));')
+    lines += ["  return 0;", "}"]
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        open(src, "w").write("\n".join(lines) + "\n")
+        subprocess.run([cc, "-I", os.path.dirname(HEADER), src, "-o", exe], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    return {tuple(l.split()[:2]): int(l.split()[2]) for l in out.splitlines()}
+
+
+@pytest.mark.parametrize("py,c", [(binding.Args, "attnres_args"), (binding.Config, "attnres_config")])
+def test_struct_layouts_match_the_header(py, c):
+    lay = _c_layout()
+    assert ctypes.sizeof(py) == lay[(c, "sizeof")]
+    for f, _ in py._fields_:
+        assert getattr(py, f).offset == lay[(c, f)], f
+
+
+def test_fp16_validation_on_host():
+    a = _layout()
+    lib = binding.load()
+    vp = ctypes.c_void_p
+    args = [vp(a["prefix"]), vp(a["add"]), vp(a["add2"]), vp(a["bank"]), vp(a["w"]), vp(a["gamma"]),
+            1e-6, vp(a["out"]), vp(a["new_prefix"])]
+    # FP16 with more than 12 snapshots is not built
+    assert lib.attnres_add_rmsnorm_f16(*args, M, 13, H, None) == -9
+    # the usual checks hold for FP16 too
+    assert lib.attnres_add_rmsnorm_f16(*args[:7], vp(a["add"]), vp(a["new_prefix"]), M, N, H, None) == -4
+    assert lib.attnres_add_rmsnorm_f16(*args, M, N, 12, None) == -2
+    # an unknown element type
+    x = binding.Args(a["prefix"], a["add"], a["add2"], a["bank"], a["w"], a["gamma"], 1e-6, a["out"],
+                     a["new_prefix"], None, M, N, H, 1, 2)
+    assert lib.attnres_launch(ctypes.byref(x), None, None) == -9
