@@ -600,14 +600,16 @@ def run_ours(args):
         return max_over_ranks(x, "cuda")
 
     # ---- the bandwidth workload, resident in HBM
-    M = args.tokens
-    inp = wl.bandwidth_inputs(device="cuda", seed=rank_seed(rank), M=M)
+    M, N = args.tokens, args.snapshots
+    default_workload = M == M_BW and N == N_BW and not args.fp16
+    inp = wl.bandwidth_inputs(device="cuda", seed=rank_seed(rank), M=M, N=N,
+                              dtype=torch.float16 if args.fp16 else torch.bfloat16)
     stream = torch.cuda.Stream()
     config = None
     if args.variant != "auto" or args.cluster or args.stages:
         config = binding.make_config(args.variant, cluster=args.cluster, stages=args.stages)
     call, ev, t0, t1, out, newp = time_bandwidth(binding, inp, args.steps, args.warmup, stream, config)
-    nbytes = algorithmic_bytes(M, N_BW, H)
+    nbytes = algorithmic_bytes(M, N, H)
 
     # soak: the same calls back to back so that the clock samples see steady load
     sampler = ClockSampler(torch.cuda.current_device())
@@ -652,7 +654,7 @@ def run_ours(args):
         chain = chain_benchmark(binding, wl)
         deep = deep_banks(binding, wl, peaks()[0])
         fp16 = fp16_tensors(binding, wl, peaks()[0])
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and default_workload:
         # the oracle on the first tokens of this same workload; the GPU's
         # outputs for those tokens are checked against it on the way
         import numpy as np
@@ -687,16 +689,20 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_s / args.steps * 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) BF16 tensors)",
-        "config": {"workload": WORKLOAD if M == M_BW else WORKLOAD.replace("M=8192", f"M={M}"), "M": M, "N": N_BW, "H": H, "add2": True,
-                   "bytes_per_call": nbytes, "l2": "inputs (2.0 GB) larger than L2, no flush",
-                   "plan": binding.attnres_plan(M, N_BW, H) if config is None else config.as_dict(),
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "fp16" if args.fp16 else "bf16",
+        "data": f"synthetic (seeded N(0,1) {'FP16' if args.fp16 else 'BF16'} tensors)",
+        "config": {"workload": WORKLOAD.replace("M=8192", f"M={M}").replace("N=12", f"N={N}")
+                   .replace("BF16", "FP16" if args.fp16 else "BF16"), "M": M, "N": N, "H": H, "add2": True,
+                   "bytes_per_call": nbytes,
+                   "l2": f"inputs ({nbytes / 1e9:.2f} GB) larger than L2, no flush" if nbytes > 2.5 * 129e6
+                   else "inputs smaller than 2.5x L2 (profiling size)",
+                   "plan": binding.attnres_plan(M, N, H) if config is None else config.as_dict(),
                    "parallelism": f"dp{ws} (each rank its own 8192 tokens)"},
         "us_per_call": round(total_s / args.steps * 1e6, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
-                     "traffic": profiled_traffic(), "algorithmic_bytes": nbytes,
+                     "traffic": profiled_traffic() if default_workload else None,
+                     "algorithmic_bytes": nbytes,
                      "avg_launch_us": round(avg_launch * 1e6, 2)},
         "e2e": e2e,
         "gpu_launches": args.steps,
@@ -729,6 +735,10 @@ def main(argv=None):
                     help="back-to-back calls before the timed region, under the clock sampler")
     ap.add_argument("--tokens", type=int, default=M_BW,
                     help="tokens of the bandwidth workload (smaller only for profiling runs)")
+    ap.add_argument("--snapshots", type=int, default=N_BW,
+                    help="bank snapshots N of the bandwidth workload (other values only for profiling)")
+    ap.add_argument("--fp16", action="store_true",
+                    help="FP16 tensors instead of BF16 (profiling)")
     ap.add_argument("--variant", default="auto", choices=("auto", "cta", "cluster", "stream", "pipe"),
                     help="pin the launch variant of the bandwidth workload (profiling)")
     ap.add_argument("--cluster", type=int, default=0)

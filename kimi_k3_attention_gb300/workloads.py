@@ -190,7 +190,8 @@ def chain_appends_after(layer: int) -> bool:
     return layer % 2 == 1 and layer <= 21
 
 
-def bandwidth_inputs(device="cuda", seed=4, M=8192, N=12, H=H_MODEL, add2=True) -> Inputs:
+def bandwidth_inputs(device="cuda", seed=4, M=8192, N=12, H=H_MODEL, add2=True,
+                     dtype=torch.bfloat16) -> Inputs:
     """M=8192 tokens, N=12, H=7168, add2 present: ~2.0 GB per call.  Drawn on
     `device` (a CUDA generator when device is a GPU) to keep set-up short."""
-    return make_inputs(M, N, H, seed=seed, add2=add2, device=device)
+    return make_inputs(M, N, H, seed=seed, add2=add2, device=device, dtype=dtype)
