@@ -13,10 +13,12 @@
 //           persistent)
 //   fold    new_prefix = bf16(prefix + bf16(add + add2)) with add.rn.f32 and
 //           cvt.rn.bf16x2.f32 written in PTX, so no fast-math flag can turn
-//           them into flush-to-zero forms (TensorRT-LLM PR #20546, "Op")
+//           them into flush-to-zero forms (TensorRT-LLM PR #20546, "Op");
+//           FP16 tensors round to FP16 instead (Fmt<kFP16>)
 //   stats   ss_i = sum v^2 and d_i = w.v for the N+1 sources, one pass of
-//           mixed-precision FMAs (BF16 operands, float32 accumulators)
-//   R1      2(N+1) partial sums: warp transpose-reduction, CTA sum in shared
+//           mixed-precision FMAs (16-bit operands, float32 accumulators)
+//   R1      2(N+1) partial sums: warp transpose-reduction (one per group of
+//           up to 16 sources, see Sums), CTA sum in shared
 //           memory, then every CTA stores its totals into the shared memory
 //           of every CTA of the cluster with st.async, each store counted on
 //           the receiver's mbarrier, which the receiver waits on
@@ -24,7 +26,8 @@
 //           totals in the same order, so all warps of all CTAs agree bitwise
 //   mix     h = sum_i alpha_i v_i from registers (no second read)
 //   R2      sum h^2: warp reduction, st.async to every CTA, mbarrier wait
-//   out     bf16(h * rsqrt(mean(h^2) + eps) * gamma) and new_prefix stored
+//   out     bf16(h * rsqrt(mean(h^2) + eps) * gamma) (FP16 for FP16 tensors)
+//           and new_prefix stored
 //
 // Every reduction has a fixed order, so results are deterministic.  Waits:
 // the CTA barrier, one cluster barrier per kernel (arrive when the exchange
@@ -50,7 +53,7 @@ struct Params {
   const uint4* gamma;
   uint4* out;
   uint4* new_prefix;      // unused when the kernel does not fold
-  uint4* h_out;           // optional BF16 copy of the mixture h (NULL: none)
+  uint4* h_out;           // optional 16-bit copy of the mixture h (NULL: none)
   long long bank_stride;  // chunks between snapshots: M * H8
   int M;
   int H8;                 // 16-byte chunks per row: H / 8
@@ -501,7 +504,7 @@ struct RegSources {
   __device__ __forceinline__ uint4 get(int i, int k) const { return v[i][k]; }
   __device__ __forceinline__ void set_new_prefix(int k, const uint4& u) { v[N][k] = u; }
   __device__ __forceinline__ uint4 new_prefix(int k) const { return v[N][k]; }
-  // Keep only the packed BF16 words alive across the reductions: without
+  // Keep only the packed 16-bit words alive across the reductions: without
   // this the compiler reuses the unpacked floats of the first pass in the
   // mixture and holds twice the registers.
   __device__ __forceinline__ void fence() {

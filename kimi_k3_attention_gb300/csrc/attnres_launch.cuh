@@ -13,7 +13,8 @@ constexpr int kMaxDevices = 64;
 // The compiled shapes of the kernel.
 //   split:  8 columns per thread, up to 256 threads (a cluster of CTAs per token)
 //   stream: 8 columns per thread, up to 224 threads, registers capped so
-//           that three CTAs fit an SM (many tokens in flight at large M)
+//           that three CTAs fit an SM (many tokens in flight at large M);
+//           deep banks have their own streaming shape (below)
 //   cta:    16 columns per thread, up to 448 threads (one CTA per token)
 constexpr int kSplitVPT = 1, kSplitMaxT = 256, kSplitMinB = 1;
 constexpr int kStreamVPT = 1, kStreamMaxT = 224, kStreamMinB = 3;
