@@ -184,10 +184,11 @@ def chain_inputs(M=8, H=H_MODEL, layers=25, seed=2546):
     return emb, p0, out
 
 
-def chain_appends_after(layer: int) -> bool:
+def chain_appends_after(layer: int, last_append: int = 21) -> bool:
     """The bank grows 1 -> 12: a copy of the carried prefix is appended after
-    every odd layer up to 21, so layers 22..24 run with N = 12."""
-    return layer % 2 == 1 and layer <= 21
+    every odd layer up to 21, so layers 22..24 run with N = 12.  A deeper
+    chain (61 layers, last_append = 59) grows the bank to 31 snapshots."""
+    return layer % 2 == 1 and layer <= last_append
 
 
 def bandwidth_inputs(device="cuda", seed=4, M=8192, N=12, H=H_MODEL, add2=True,

@@ -125,8 +125,8 @@ def test_fold_sweep_all_patterns():
 
 # ---------------------------------------------------------------- 25-layer chain
 
-def _chain_gpu(fused, M=8):
-    emb, p0, layers = wl.chain_inputs(M=M)
+def _chain_gpu(fused, M=8, layers=25, last_append=21):
+    emb, p0, layers = wl.chain_inputs(M=M, layers=layers)
     dev = "cuda"
     bank = [emb.to(dev)]
     P = p0.to(dev)
@@ -145,16 +145,19 @@ def _chain_gpu(fused, M=8):
         P = newp
         taps.append(u16(out))
         prefixes.append(u16(newp))
-        if wl.chain_appends_after(li):
+        if wl.chain_appends_after(li, last_append):
             bank.append(P.clone())
     torch.cuda.synchronize()
     return u16(torch.stack(bank)), prefixes, taps
 
 
-def test_chain_fused_equals_eager_bitwise_and_oracle():
-    bf, pf, tf = _chain_gpu(True)
-    be, pe, te = _chain_gpu(False)
-    assert bf.shape[0] == 12
+@pytest.mark.parametrize("layers,last_append,depth", [(25, 21, 12), (61, 59, 31)])
+def test_chain_fused_equals_eager_bitwise_and_oracle(layers, last_append, depth):
+    """The 25-layer chain of the pages (bank 1 -> 12), and a 61-layer chain
+    whose bank grows to 31 snapshots (the deep-bank kernels in the hand-off)."""
+    bf, pf, tf = _chain_gpu(True, layers=layers, last_append=last_append)
+    be, pe, te = _chain_gpu(False, layers=layers, last_append=last_append)
+    assert bf.shape[0] == depth
     assert (bf == be).all()
     for a, b in zip(pf, pe):
         assert (a == b).all()
@@ -162,17 +165,17 @@ def test_chain_fused_equals_eager_bitwise_and_oracle():
         assert (a == b).all()
     # and layer by layer against the oracle on the same inputs
     from oracle import attnres_add_rmsnorm as oop, check_out
-    emb, p0, layers = wl.chain_inputs(M=8)
+    emb, p0, chain = wl.chain_inputs(M=8, layers=layers)
     bank = [u16(emb)]
     P = u16(p0)
-    for li, L in enumerate(layers):
+    for li, L in enumerate(chain):
         npb, out, bound = oop(P, u16(L.routed), u16(L.shared), np.stack(bank), u16(L.w),
                               u16(L.gamma), wl.EPS)
         assert (npb == pf[li]).all(), li
         r = check_out(tf[li], out, bound)
         assert r["ok"], (li, r)
         P = npb
-        if wl.chain_appends_after(li):
+        if wl.chain_appends_after(li, last_append):
             bank.append(P.copy())
 
 

@@ -10,6 +10,7 @@ Eager: PyTorch adds routed + shared in BF16 first, then the op runs with one
 addend.  P <- new_prefix; after every odd layer up to 21 a copy of P joins
 the bank (N grows 1 -> 12); every layer's out is the tap."""
 import numpy as np
+import pytest
 import torch
 
 from kimi_k3_attention_gb300 import workloads as wl
@@ -20,7 +21,7 @@ def _u(t):
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def run_chain_oracle(H=256, M=4, layers=25, fused=True):
+def run_chain_oracle(H=256, M=4, layers=25, fused=True, last_append=21):
     torch.set_flush_denormal(False)
     emb, p0, L = wl.chain_inputs(M=M, H=H, layers=layers)
     bank = [_u(emb)]
@@ -35,7 +36,7 @@ def run_chain_oracle(H=256, M=4, layers=25, fused=True):
         P = newp
         taps.append(out)
         prefixes.append(newp)
-        if wl.chain_appends_after(li):
+        if wl.chain_appends_after(li, last_append):
             bank.append(P.copy())
     return np.stack(bank), prefixes, taps
 
@@ -50,10 +51,19 @@ def test_chain_schedule_grows_bank_to_twelve():
     assert ns[0] == 1 and ns[-1] == 12 and ns[22:] == [12, 12, 12]
 
 
-def test_chain_fused_equals_eager_bitwise():
-    bank_f, p_f, t_f = run_chain_oracle(fused=True)
-    bank_e, p_e, t_e = run_chain_oracle(fused=False)
-    assert bank_f.shape[0] == 12
+def test_deep_chain_schedule_grows_bank_to_thirty_one():
+    n = 1
+    for li in range(61):
+        if wl.chain_appends_after(li, 59):
+            n += 1
+    assert n == 31
+
+
+@pytest.mark.parametrize("layers,last_append,depth", [(25, 21, 12), (61, 59, 31)])
+def test_chain_fused_equals_eager_bitwise(layers, last_append, depth):
+    bank_f, p_f, t_f = run_chain_oracle(fused=True, layers=layers, last_append=last_append)
+    bank_e, p_e, t_e = run_chain_oracle(fused=False, layers=layers, last_append=last_append)
+    assert bank_f.shape[0] == depth
     assert (bank_f == bank_e).all()
     for a, b in zip(p_f, p_e):
         assert (a == b).all()
