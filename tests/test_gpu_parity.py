@@ -2,6 +2,7 @@
 seeded workloads: new_prefix bit-exact, out within the tolerance of
 oracle/tolerance.py (2 BF16 ulp with a 2^-16 floor; |delta| <= 1.5e-2 where
 |out| <= 4)."""
+import math
 import os
 
 import numpy as np
@@ -557,3 +558,15 @@ def test_next_token_prefetch_identical(prefetch):
     ref = run_gpu(inp, binding.make_config("stream", cluster=7, grid_tokens=5, prefetch=-1))
     assert (got[0] == ref[0]).all() and (got[1] == ref[1]).all()
     assert_parity(inp, *got)
+
+
+@pytest.mark.parametrize("eps", [1e-12, 1e-2, 1.0, 1e3])
+@pytest.mark.parametrize("cfg", [None, binding.make_config("stream", cluster=7),
+                                 binding.make_config("cta")], ids=cfg_name)
+def test_eps_range(eps, cfg):
+    """eps from negligible to dominant (1e3 >> mean(v^2) = 1: both norms are
+    then close to a plain 1/sqrt(eps) scaling); the oracle takes the same
+    float32 eps."""
+    inp = wl.make_inputs(6, 7, H, seed=900 + round(math.log10(eps)), eps=eps)
+    np_, out = run_gpu(inp, config=cfg)
+    assert_parity(inp, np_, out, label=f"eps={eps} {cfg_name(cfg)}")
