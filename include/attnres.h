@@ -122,7 +122,8 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *                 three CTAs share an SM;
  *             Variants 1 and 4 exist for N <= 12 only.  For N > 12
  *             variant 3 takes at most 128 threads, registers capped so
- *             that three to five CTAs (fewer as N grows) share an SM.
+ *             that four or five CTAs share an SM (from N = 23 on with
+ *             bank rows 16..N-1 in dynamic shared memory).
  *             4 = persistent and pipelined (the large-M streaming kernel): a
  *                 grid of as many clusters as fit the GPU at once walks the
  *                 tokens; every thread copies its chunks of the token

@@ -357,9 +357,10 @@ cudaError_t launch_deep(int mode, const Params& p, dim3 g, int t, int c, bool pd
   constexpr int VPT = STREAM ? kStreamVPT : kSplitVPT;
   constexpr int MAXT = STREAM ? kDeepStreamMaxT : kSplitMaxT;
   constexpr int MINB = STREAM ? deep_minb(N) : kSplitMinB;
-  return mode == kFoldAdd2 ? launch_fused<N, kFoldAdd2, VPT, MAXT, MINB>(p, g, t, c, pdl, s)
-         : mode == kFoldAdd ? launch_fused<N, kFoldAdd, VPT, MAXT, MINB>(p, g, t, c, pdl, s)
-                            : launch_fused<N, kNoFold, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
+  constexpr int NR = STREAM ? deep_nr(N) : N;
+  return mode == kFoldAdd2 ? launch_fused<N, kFoldAdd2, VPT, MAXT, MINB, kBF16, NR>(p, g, t, c, pdl, s)
+         : mode == kFoldAdd ? launch_fused<N, kFoldAdd, VPT, MAXT, MINB, kBF16, NR>(p, g, t, c, pdl, s)
+                            : launch_fused<N, kNoFold, VPT, MAXT, MINB, kBF16, NR>(p, g, t, c, pdl, s);
 }
 
 template <bool STREAM>

@@ -516,6 +516,29 @@ struct RegSources {
   }
 };
 
+// Deep banks in the streaming shape: bank[0..NR-1] and the updated prefix in
+// registers, bank[NR..N-1] in this thread's own slots of a shared-memory
+// area (cp.async copies, read twice: sums, then mixture).
+template <int N, int NR>
+struct HybridSources {
+  uint4 (&v)[NR + 1][1];   // bank[0..NR-1]; index NR holds the updated prefix
+  uint32_t slot0;          // shared address of this thread's bank[NR] slot
+  uint32_t step;           // bytes between consecutive rows
+  bool ok;
+  __device__ __forceinline__ uint4 get(int i, int) const {
+    if (i < NR) return v[i][0];
+    if (i == N) return v[NR][0];
+    return ok ? lds16(slot0 + static_cast<uint32_t>(i - NR) * step) : make_uint4(0, 0, 0, 0);
+  }
+  __device__ __forceinline__ void set_new_prefix(int, const uint4& u) { v[NR][0] = u; }
+  __device__ __forceinline__ uint4 new_prefix(int) const { return v[NR][0]; }
+  __device__ __forceinline__ void fence() {
+#pragma unroll
+    for (int i = 0; i <= NR; ++i)
+      asm volatile("" : "+r"(v[i][0].x), "+r"(v[i][0].y), "+r"(v[i][0].z), "+r"(v[i][0].w));
+  }
+};
+
 template <int N>
 struct SmemSources {
   uint32_t bank0;     // shared address of this thread's bank[0] slot
@@ -736,9 +759,14 @@ __device__ __forceinline__ Thread thread_info() {
 
 // Loads straight to registers; each cluster handles tokens blockIdx.y,
 // blockIdx.y + gridDim.y, ...  DT is the element format of every tensor.
-template <int N, int MODE, int VPT, int MAXT, int MINB, int DT = kBF16>
+// NR < N keeps bank rows NR..N-1 in shared memory instead (HybridSources;
+// one column chunk per thread).
+template <int N, int MODE, int VPT, int MAXT, int MINB, int DT = kBF16, int NR = N>
 __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params p) {
+  constexpr bool HYB = NR < N;
+  static_assert(!HYB || VPT == 1, "shared-memory rows take one chunk per thread");
   __shared__ Exchange<Sums<N>::G> x;
+  extern __shared__ __align__(16) uint4 hyb[];   // [N - NR][blockDim.x] when HYB
   Thread t = thread_info();
   const int c0 = static_cast<int>(t.crank) * p.cpc;
   const int cend = min(c0 + p.cpc, p.H8);
@@ -792,7 +820,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   bool first = true;
   for (int m = blockIdx.y; m < p.M; m += gridDim.y) {
     const size_t row = static_cast<size_t>(m) * p.H8;
-    uint4 v[N + 1][VPT];
+    uint4 v[NR + 1][VPT];
     uint4 pr[VPT], ad[VPT], ad2[VPT];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -801,8 +829,18 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
       ad[k] = (MODE != kNoFold && ok[k]) ? ld_stream(p.add + row + jj[k]) : z;
       ad2[k] = (MODE == kFoldAdd2 && ok[k]) ? ld_stream(p.add2 + row + jj[k]) : z;
 #pragma unroll
-      for (int i = 0; i < N; ++i)
+      for (int i = 0; i < NR; ++i)
         v[i][k] = ok[k] ? ld_stream(p.bank + i * p.bank_stride + row + jj[k]) : z;
+    }
+    const uint32_t hyb0 = smem_u32(hyb) + threadIdx.x * 16u;
+    const uint32_t hstep = blockDim.x * 16u;
+    if constexpr (HYB) {
+      if (ok[0]) {
+#pragma unroll
+        for (int i = NR; i < N; ++i)
+          cp_async16(hyb0 + static_cast<uint32_t>(i - NR) * hstep, p.bank + i * p.bank_stride + row + jj[0]);
+      }
+      cp_async_commit();
     }
     // While this token is reduced, let L2 fetch this CTA's rows of the next
     // token it will take: the requests keep HBM busy during the reductions
@@ -821,8 +859,14 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // grid is past its loads; it still waits for this grid to finish.
     griddep_launch_dependents();
     if (!early_init && m == static_cast<int>(blockIdx.y)) exchange_init<Sums<N>::total>(x, t, p);
-    RegSources<N, VPT> src{v};
-    token_epilogue<N, MODE, VPT, DT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
+    if constexpr (HYB) {
+      cp_async_wait<0>();   // this thread's own slots: no barrier needed
+      HybridSources<N, NR> src{v, hyb0, hstep, ok[0]};
+      token_epilogue<N, MODE, VPT, DT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
+    } else {
+      RegSources<N, VPT> src{v};
+      token_epilogue<N, MODE, VPT, DT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
+    }
   }
   exchange_exit(t, p);
 }
@@ -927,7 +971,7 @@ __global__ void __launch_bounds__(256) attnres_tail_add_kernel(const uint4* __re
 }
 
 // Host-side launchers of one instantiation (defined in attnres_launch.cuh).
-template <int N, int MODE, int VPT, int MAXT, int MINB, int DT = kBF16>
+template <int N, int MODE, int VPT, int MAXT, int MINB, int DT = kBF16, int NR = N>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
                          cudaStream_t s);
 template <int N, bool ADD2, int STAGES>

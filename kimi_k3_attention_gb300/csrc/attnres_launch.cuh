@@ -22,34 +22,47 @@ constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 
 // Every shape is compiled for N <= kShallowMaxN.  Deeper banks (up to
 // ATTNRES_MAX_N) have the split shape and a streaming shape of their own:
-// up to 128 threads, registers capped so that deep_minb(N) CTAs share an SM
-// (GB300, M = 8192: 4.7-6.1 TB/s for N = 13..31 against 3.3-4.1 TB/s
-// uncapped; spills stay within a few dozen bytes).
+// up to 128 threads, registers capped so that deep_minb(N) CTAs share an SM,
+// and from 23 snapshots on the bank rows past deep_nr(N) = 16 held in shared
+// memory instead of registers (GB300, M = 8192: 4.9-6.1 TB/s for N = 13..31,
+// against 3.3-4.1 TB/s uncapped and 4.6-4.9 TB/s at N = 24..31 with every
+// row in registers; spills stay within a few dozen bytes).
 constexpr int kShallowMaxN = 12;
 constexpr int kDeepStreamMaxT = 128;
-constexpr int deep_minb(int n) { return n <= 16 ? 5 : n <= 24 ? 4 : 3; }
+constexpr int deep_minb(int n) { return n <= 16 ? 5 : 4; }
+constexpr int deep_nr(int n) { return n >= 23 ? 16 : n; }
 
-template <int N, int MODE, int VPT, int MAXT, int MINB, int DT>
+template <int N, int MODE, int VPT, int MAXT, int MINB, int DT, int NR>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
                          cudaStream_t s) {
-  auto kern = attnres_fused_kernel<N, MODE, VPT, MAXT, MINB, DT>;
-  // Cluster sizes above 8 need an opt-in per function and device.
+  auto kern = attnres_fused_kernel<N, MODE, VPT, MAXT, MINB, DT, NR>;
+  // Cluster sizes above 8 need an opt-in per function and device, and so
+  // does dynamic shared memory above the default limit (the limit set only
+  // grows).
   static std::atomic<unsigned char> opted[kMaxDevices];
-  if (cluster > 8) {
+  static std::atomic<int> smem_set[kMaxDevices];
+  const int dyn = (N - NR) * threads * 16;
+  if (cluster > 8 || dyn > 0) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!opted[dev].load(std::memory_order_acquire)) {
+    if (cluster > 8 && !opted[dev].load(std::memory_order_acquire)) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
       opted[dev].store(1, std::memory_order_release);
+    }
+    if (dyn > smem_set[dev].load(std::memory_order_acquire)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+      if (e != cudaSuccess) return e;
+      smem_set[dev].store(dyn, std::memory_order_release);
     }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  // bank rows NR..N-1 in shared memory
+  cfg.dynamicSmemBytes = static_cast<size_t>(N - NR) * threads * 16u;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -168,6 +181,10 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   DEF template cudaError_t launch_fused<N, MODE, VPT, MAXT, MINB, DT>(const Params&, dim3, int, \
                                                                       int, bool, cudaStream_t);
 
+#define ATTNRES_FUSED_NR(DEF, N, MODE, VPT, MAXT, MINB, NR)                                  \
+  DEF template cudaError_t launch_fused<N, MODE, VPT, MAXT, MINB, kBF16, NR>(                   \
+      const Params&, dim3, int, int, bool, cudaStream_t);
+
 #define ATTNRES_PIPE(DEF, N, ADD2, STAGES)                                          \
   DEF template cudaError_t launch_pipe<N, ADD2, STAGES>(const Params&, dim3, int, int, bool, \
                                                         cudaStream_t);
@@ -193,9 +210,9 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   ATTNRES_FUSED(DEF, N, kFoldAdd2, kSplitVPT, kSplitMaxT, kSplitMinB)              \
   ATTNRES_FUSED(DEF, N, kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB)               \
   ATTNRES_FUSED(DEF, N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB)                \
-  ATTNRES_FUSED(DEF, N, kFoldAdd2, kStreamVPT, kDeepStreamMaxT, deep_minb(N))      \
-  ATTNRES_FUSED(DEF, N, kFoldAdd, kStreamVPT, kDeepStreamMaxT, deep_minb(N))       \
-  ATTNRES_FUSED(DEF, N, kNoFold, kStreamVPT, kDeepStreamMaxT, deep_minb(N))
+  ATTNRES_FUSED_NR(DEF, N, kFoldAdd2, kStreamVPT, kDeepStreamMaxT, deep_minb(N), deep_nr(N)) \
+  ATTNRES_FUSED_NR(DEF, N, kFoldAdd, kStreamVPT, kDeepStreamMaxT, deep_minb(N), deep_nr(N))  \
+  ATTNRES_FUSED_NR(DEF, N, kNoFold, kStreamVPT, kDeepStreamMaxT, deep_minb(N), deep_nr(N))
 
 // FP16 tensors, N <= 12: the split and streaming shapes, with the fold
 // (add2 present or not) and without.
