@@ -274,7 +274,7 @@ def time_bandwidth(binding, inp, steps, warmup, stream, config=None):
     return call, ev, t_all0, t_all1, out, newp
 
 
-def decode_latencies(binding, wl, reps=200, replays=5):
+def decode_latencies(binding, wl, reps=200, replays=20):
     """Microseconds per call in the decode window (H=7168, both addends), from
     CUDA-graph replays of back-to-back calls on one stream:
       warm: `reps` calls on the same buffers (inputs L2-resident);
@@ -341,7 +341,7 @@ def decode_latencies(binding, wl, reps=200, replays=5):
     return res
 
 
-def _graph_us(build_calls, s, replays=5):
+def _graph_us(build_calls, s, replays=20):
     """Capture build_calls() (which enqueues `n` calls on stream s and returns
     n) in a CUDA graph; median microseconds per call over `replays`."""
     import torch
