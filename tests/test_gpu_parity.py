@@ -448,6 +448,46 @@ def test_random_configurations(case):
     assert_parity(inp, gnp, gout, label=str(case))
 
 
+def _random_wide_cases(n=40, seed=2612):
+    """Deep banks (N up to 31) and FP16 tensors (N up to 12) in the split and
+    streaming shapes, with random cluster sizes, grid strides and prefetch
+    modes."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        H8 = int(rng.choice([1, 3, 40, 257, 896, 897, 2048]))
+        M = int(rng.choice([1, 5, 33, 130]))
+        fp16 = bool(rng.integers(0, 2))
+        N = int(rng.integers(0, 13)) if fp16 else int(rng.integers(13, 32))
+        add2 = bool(rng.integers(0, 2))
+        variant = str(rng.choice(["auto", "cluster", "stream"]))
+        lim = {"cluster": 256, "stream": 224 if N <= 12 else 128, "auto": None}[variant]
+        cluster = 0
+        if lim is not None:
+            ok = [c for c in range(1, 17) if -(-(-(-H8 // c)) // 32) * 32 <= lim]
+            if not ok:
+                continue
+            cluster = int(rng.choice(ok))
+        gt = int(rng.choice([0, 0, 1, 3]))
+        pf = int(rng.choice([0, -1, 1, 4, 5])) if variant != "auto" else 0
+        cases.append((M, N, 8 * H8, add2, fp16, variant, cluster, gt, pf, int(rng.integers(0, 10 ** 6))))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_wide_cases(), ids=lambda c: "M{}-N{}-H{}-{}-{}-{}{}-g{}-p{}".format(
+    c[0], c[1], c[2], "a2" if c[3] else "a1", "f16" if c[4] else "bf16", c[5], c[6], c[7], c[8]))
+def test_random_deep_and_fp16_configurations(case):
+    M, N, Hs, add2, fp16, variant, cluster, gt, pf, seed = case
+    inp = wl.make_inputs(M, max(N, 1), Hs, seed=seed, add2=add2,
+                         dtype=torch.float16 if fp16 else torch.bfloat16)
+    if N == 0:
+        inp.bank = inp.bank[:0]
+    cfg = None if variant == "auto" else binding.make_config(variant, cluster=cluster, grid_tokens=gt,
+                                                             prefetch=pf)
+    gnp, gout = run_gpu(inp, cfg)
+    assert_parity(inp, gnp, gout, label=str(case))
+
+
 def test_all_zero_sources():
     """Every source zero: sums of squares are 0, the norms divide by sqrt(eps),
     alpha is uniform and out is exactly zero."""
