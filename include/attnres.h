@@ -70,7 +70,7 @@ typedef enum {
   ATTNRES_ERR_CUDA = -6,    /* a CUDA runtime call failed                  */
   ATTNRES_ERR_DEVICE = -7,  /* the current device is not compute 10.3      */
   ATTNRES_ERR_CONFIG = -8,  /* a forced launch configuration is invalid    */
-  ATTNRES_ERR_DTYPE = -9    /* unknown element type, or FP16 with N > 12   */
+  ATTNRES_ERR_DTYPE = -9    /* unknown element type                        */
 } attnres_status;
 
 /* Element type of every tensor of a call. */
@@ -194,9 +194,9 @@ int attnres_add_rmsnorm_tap(const void* prefix, const void* add, const void* add
  * (float32 additions, round to nearest even, FP16 subnormals kept, overflow
  * to infinity), out = fp16(h / sqrt(mean(h^2) + eps) * gamma).  The PR's
  * fused window is BF16 only (section "Model"); this is the same op for a
- * model kept in FP16.  0 <= N <= 12; N > 12 returns ATTNRES_ERR_DTYPE.
- * Variants 2 and 3 only (attnres_launch with dtype ATTNRES_DTYPE_FP16 takes
- * the tap and the attention-residual alone too).
+ * model kept in FP16.  0 <= N <= 31, as for BF16.  Variants 2 and 3 only
+ * (attnres_launch with dtype ATTNRES_DTYPE_FP16 takes the tap and the
+ * attention-residual alone too).
  */
 int attnres_add_rmsnorm_f16(const void* prefix, const void* add, const void* add2,
                             const void* bank, const void* w, const void* gamma,

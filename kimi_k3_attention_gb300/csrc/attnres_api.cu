@@ -21,6 +21,9 @@ ATTNRES_UNIT_G(extern)
 ATTNRES_UNIT_H(extern)
 ATTNRES_UNIT_I(extern)
 ATTNRES_UNIT_J(extern)
+ATTNRES_UNIT_L(extern)
+ATTNRES_UNIT_M(extern)
+ATTNRES_UNIT_N(extern)
 
 namespace {
 
@@ -121,7 +124,6 @@ int validate(const Args& a) {
   if (a.fold && (!a.add || !a.new_prefix)) return ATTNRES_ERR_NULL;
   int st = validate_shape(a.M, a.N, a.H);
   if (st != ATTNRES_OK) return st;
-  if (a.dtype == ATTNRES_DTYPE_FP16 && a.N > kShallowMaxN) return ATTNRES_ERR_DTYPE;
   if (!(a.eps > 0.f) || !isfinite(a.eps)) return ATTNRES_ERR_EPS;
   const void* add = a.fold ? a.add : nullptr;
   const void* add2 = a.fold ? a.add2 : nullptr;
@@ -350,25 +352,25 @@ cudaError_t dispatch_fp16(int N, int mode, const Params& p, dim3 g, int t, int c
 }
 
 // Deep banks: the split shape (STREAM false) or the deep streaming shape,
-// with or without the fold.
-template <int N, bool STREAM>
+// with or without the fold, element format DT.
+template <int N, bool STREAM, int DT>
 cudaError_t launch_deep(int mode, const Params& p, dim3 g, int t, int c, bool pdl,
                         cudaStream_t s) {
   constexpr int VPT = STREAM ? kStreamVPT : kSplitVPT;
   constexpr int MAXT = STREAM ? kDeepStreamMaxT : kSplitMaxT;
   constexpr int MINB = STREAM ? deep_minb(N) : kSplitMinB;
   constexpr int NR = STREAM ? deep_nr(N) : N;
-  return mode == kFoldAdd2 ? launch_fused<N, kFoldAdd2, VPT, MAXT, MINB, kBF16, NR>(p, g, t, c, pdl, s)
-         : mode == kFoldAdd ? launch_fused<N, kFoldAdd, VPT, MAXT, MINB, kBF16, NR>(p, g, t, c, pdl, s)
-                            : launch_fused<N, kNoFold, VPT, MAXT, MINB, kBF16, NR>(p, g, t, c, pdl, s);
+  return mode == kFoldAdd2 ? launch_fused<N, kFoldAdd2, VPT, MAXT, MINB, DT, NR>(p, g, t, c, pdl, s)
+         : mode == kFoldAdd ? launch_fused<N, kFoldAdd, VPT, MAXT, MINB, DT, NR>(p, g, t, c, pdl, s)
+                            : launch_fused<N, kNoFold, VPT, MAXT, MINB, DT, NR>(p, g, t, c, pdl, s);
 }
 
-template <bool STREAM>
+template <bool STREAM, int DT>
 cudaError_t dispatch_deep(int N, int mode, const Params& p, dim3 g, int t, int c, bool pdl,
                           cudaStream_t s) {
 #define ATTNRES_CASE(n) \
   case n:               \
-    return launch_deep<n, STREAM>(mode, p, g, t, c, pdl, s);
+    return launch_deep<n, STREAM, DT>(mode, p, g, t, c, pdl, s);
   switch (N) {
     ATTNRES_CASE(13) ATTNRES_CASE(14) ATTNRES_CASE(15) ATTNRES_CASE(16)
     ATTNRES_CASE(17) ATTNRES_CASE(18) ATTNRES_CASE(19) ATTNRES_CASE(20)
@@ -436,16 +438,19 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   const bool pdl = c.pdl >= 0;
   cudaError_t e;
   const int mode = !a.fold ? kNoFold : has_add2 ? kFoldAdd2 : kFoldAdd;
-  if (a.dtype == ATTNRES_DTYPE_FP16 && c.variant == 2)
+  const bool fp16 = a.dtype == ATTNRES_DTYPE_FP16;
+  if (a.N > kShallowMaxN && c.variant == 2)
+    e = fp16 ? dispatch_deep<false, kFP16>(a.N, mode, p, grid, c.threads, c.cluster, pdl, s)
+             : dispatch_deep<false, kBF16>(a.N, mode, p, grid, c.threads, c.cluster, pdl, s);
+  else if (a.N > kShallowMaxN)
+    e = fp16 ? dispatch_deep<true, kFP16>(a.N, mode, p, grid, c.threads, c.cluster, pdl, s)
+             : dispatch_deep<true, kBF16>(a.N, mode, p, grid, c.threads, c.cluster, pdl, s);
+  else if (fp16 && c.variant == 2)
     e = dispatch_fp16<kSplitVPT, kSplitMaxT, kSplitMinB>(a.N, mode, p, grid, c.threads, c.cluster,
                                                          pdl, s);
-  else if (a.dtype == ATTNRES_DTYPE_FP16)
+  else if (fp16)
     e = dispatch_fp16<kStreamVPT, kStreamMaxT, kStreamMinB>(a.N, mode, p, grid, c.threads,
                                                             c.cluster, pdl, s);
-  else if (a.N > kShallowMaxN && c.variant == 2)
-    e = dispatch_deep<false>(a.N, mode, p, grid, c.threads, c.cluster, pdl, s);
-  else if (a.N > kShallowMaxN)
-    e = dispatch_deep<true>(a.N, mode, p, grid, c.threads, c.cluster, pdl, s);
   else if (!a.fold && c.variant == 2)
     e = dispatch_nofold<kSplitVPT, kSplitMaxT, kSplitMinB>(a.N, p, grid, c.threads, c.cluster, pdl, s);
   else if (!a.fold)
@@ -594,7 +599,7 @@ extern "C" const char* attnres_status_string(int status) {
     case ATTNRES_ERR_CUDA: return "a CUDA runtime call failed (see attnres_last_cuda_error)";
     case ATTNRES_ERR_DEVICE: return "the current device is not a compute capability 10.3 GPU";
     case ATTNRES_ERR_CONFIG: return "invalid launch configuration";
-    case ATTNRES_ERR_DTYPE: return "unsupported element type: BF16, or FP16 with N <= 12";
+    case ATTNRES_ERR_DTYPE: return "unsupported element type: BF16 or FP16";
     default: return "unknown status";
   }
 }

@@ -181,8 +181,8 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   DEF template cudaError_t launch_fused<N, MODE, VPT, MAXT, MINB, DT>(const Params&, dim3, int, \
                                                                       int, bool, cudaStream_t);
 
-#define ATTNRES_FUSED_NR(DEF, N, MODE, VPT, MAXT, MINB, NR)                                  \
-  DEF template cudaError_t launch_fused<N, MODE, VPT, MAXT, MINB, kBF16, NR>(                   \
+#define ATTNRES_FUSED_NR(DEF, N, MODE, VPT, MAXT, MINB, DT, NR)                              \
+  DEF template cudaError_t launch_fused<N, MODE, VPT, MAXT, MINB, DT, NR>(                      \
       const Params&, dim3, int, int, bool, cudaStream_t);
 
 #define ATTNRES_PIPE(DEF, N, ADD2, STAGES)                                          \
@@ -205,14 +205,16 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   ATTNRES_FUSED(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, kStreamMinB)
 
 // Deep banks, 13 <= N <= 31: the split shape and the deep streaming shape,
-// with the fold (add2 present or not) and without.
-#define ATTNRES_INSTANTIATE_DEEP(DEF, N)                                           \
-  ATTNRES_FUSED(DEF, N, kFoldAdd2, kSplitVPT, kSplitMaxT, kSplitMinB)              \
-  ATTNRES_FUSED(DEF, N, kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB)               \
-  ATTNRES_FUSED(DEF, N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB)                \
-  ATTNRES_FUSED_NR(DEF, N, kFoldAdd2, kStreamVPT, kDeepStreamMaxT, deep_minb(N), deep_nr(N)) \
-  ATTNRES_FUSED_NR(DEF, N, kFoldAdd, kStreamVPT, kDeepStreamMaxT, deep_minb(N), deep_nr(N))  \
-  ATTNRES_FUSED_NR(DEF, N, kNoFold, kStreamVPT, kDeepStreamMaxT, deep_minb(N), deep_nr(N))
+// with the fold (add2 present or not) and without, for element format DT.
+#define ATTNRES_INSTANTIATE_DEEP_DT(DEF, N, DT)                                               \
+  ATTNRES_FUSED_DT(DEF, N, kFoldAdd2, kSplitVPT, kSplitMaxT, kSplitMinB, DT)                  \
+  ATTNRES_FUSED_DT(DEF, N, kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB, DT)                   \
+  ATTNRES_FUSED_DT(DEF, N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB, DT)                    \
+  ATTNRES_FUSED_NR(DEF, N, kFoldAdd2, kStreamVPT, kDeepStreamMaxT, deep_minb(N), DT, deep_nr(N)) \
+  ATTNRES_FUSED_NR(DEF, N, kFoldAdd, kStreamVPT, kDeepStreamMaxT, deep_minb(N), DT, deep_nr(N))  \
+  ATTNRES_FUSED_NR(DEF, N, kNoFold, kStreamVPT, kDeepStreamMaxT, deep_minb(N), DT, deep_nr(N))
+#define ATTNRES_INSTANTIATE_DEEP(DEF, N) ATTNRES_INSTANTIATE_DEEP_DT(DEF, N, kBF16)
+#define ATTNRES_INSTANTIATE_DEEP_FP16(DEF, N) ATTNRES_INSTANTIATE_DEEP_DT(DEF, N, kFP16)
 
 // FP16 tensors, N <= 12: the split and streaming shapes, with the fold
 // (add2 present or not) and without.
@@ -269,6 +271,19 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   ATTNRES_INSTANTIATE_DEEP(DEF, 27) ATTNRES_INSTANTIATE_DEEP(DEF, 28)                   \
   ATTNRES_INSTANTIATE_DEEP(DEF, 29) ATTNRES_INSTANTIATE_DEEP(DEF, 30)                   \
   ATTNRES_INSTANTIATE_DEEP(DEF, 31)
+#define ATTNRES_UNIT_L(DEF)                                                             \
+  ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 13) ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 14)         \
+  ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 15) ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 16)         \
+  ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 17) ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 18)
+#define ATTNRES_UNIT_M(DEF)                                                             \
+  ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 19) ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 20)         \
+  ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 21) ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 22)         \
+  ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 23) ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 24)
+#define ATTNRES_UNIT_N(DEF)                                                             \
+  ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 25) ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 26)         \
+  ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 27) ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 28)         \
+  ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 29) ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 30)         \
+  ATTNRES_INSTANTIATE_DEEP_FP16(DEF, 31)
 #define ATTNRES_UNIT_I(DEF)                                                             \
   ATTNRES_INSTANTIATE_FP16(DEF, 0) ATTNRES_INSTANTIATE_FP16(DEF, 1)                     \
   ATTNRES_INSTANTIATE_FP16(DEF, 2) ATTNRES_INSTANTIATE_FP16(DEF, 3)                     \

@@ -2,8 +2,9 @@
 
 The fused window of TensorRT-LLM PR #20546 (section "Model") is BF16; the
 library runs the same op on FP16 tensors (every tensor FP16, both fold
-additions rounded to FP16).  The oracle takes the FP16 codec; new_prefix must
-be bit-exact, out within 2 FP16 ulp (with the float32 floor)."""
+additions rounded to FP16), for every N the BF16 path takes.  The oracle
+takes the FP16 codec; new_prefix must be bit-exact, out within 2 FP16 ulp
+(with the float32 floor)."""
 import os
 
 import numpy as np
@@ -203,13 +204,16 @@ def test_fp16_rejects_uncompiled_shapes(cfg):
     assert e.value.status == -8
 
 
-def test_fp16_deep_bank_rejected():
-    inp = wl.make_inputs(2, 13, 64, seed=6700, dtype=F16)
-    d = inp.to("cuda")
-    out, newp = torch.empty_like(d.prefix), torch.empty_like(d.prefix)
-    with pytest.raises(binding.AttnResError) as e:
-        binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps, out, newp)
-    assert e.value.status == -9
+@pytest.mark.parametrize("N", [13, 20, 23, 31])
+@pytest.mark.parametrize("M", [1, 64, 300])
+def test_fp16_deep_banks(M, N):
+    """FP16 tensors with more than 12 snapshots: the deep split shape up to 32
+    tokens, the deep streaming shape (shared-memory rows from N = 23) above."""
+    inp = wl.make_inputs(M, N, H, seed=6700 + M + N, dtype=F16)
+    np_, out = run_gpu(inp)
+    assert_parity(inp, np_, out, label=f"M={M} N={N}")
+    np2, out2 = run_gpu(inp, config=binding.make_config("stream", cluster=8, grid_tokens=7))
+    assert_parity(inp, np2, out2, label=f"stream M={M} N={N}")
 
 
 def test_mixed_dtypes_rejected_by_the_binding():

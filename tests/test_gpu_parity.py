@@ -449,7 +449,7 @@ def test_random_configurations(case):
 
 
 def _random_wide_cases(n=40, seed=2612):
-    """Deep banks (N up to 31) and FP16 tensors (N up to 12) in the split and
+    """Deep banks (N up to 31) and FP16 tensors (N up to 31) in the split and
     streaming shapes, with random cluster sizes, grid strides and prefetch
     modes."""
     rng = np.random.default_rng(seed)
@@ -458,7 +458,7 @@ def _random_wide_cases(n=40, seed=2612):
         H8 = int(rng.choice([1, 3, 40, 257, 896, 897, 2048]))
         M = int(rng.choice([1, 5, 33, 130]))
         fp16 = bool(rng.integers(0, 2))
-        N = int(rng.integers(0, 13)) if fp16 else int(rng.integers(13, 32))
+        N = int(rng.integers(0, 32)) if fp16 else int(rng.integers(13, 32))
         add2 = bool(rng.integers(0, 2))
         variant = str(rng.choice(["auto", "cluster", "stream"]))
         lim = {"cluster": 256, "stream": 224 if N <= 12 else 128, "auto": None}[variant]
