@@ -25,13 +25,18 @@ def _restore():
     binding.device_status(clear=True)
 
 
-@pytest.mark.parametrize("cfg", [binding.make_config("cluster", cluster=4),
-                                 binding.make_config("cluster", cluster=16),
-                                 binding.make_config("pipe", cluster=4, grid_tokens=2),
-                                 binding.make_config("cta")],
-                         ids=["cluster4", "cluster16", "pipe4", "cta"])
-def test_exchange_wait_expires_and_reports(cfg):
-    inp = wl.make_inputs(5, 3, H, seed=81).to("cuda")
+@pytest.mark.parametrize("cfg,N,dtype", [
+    (binding.make_config("cluster", cluster=4), 3, torch.bfloat16),
+    (binding.make_config("cluster", cluster=16), 3, torch.bfloat16),
+    (binding.make_config("pipe", cluster=4, grid_tokens=2), 3, torch.bfloat16),
+    (binding.make_config("cta"), 3, torch.bfloat16),
+    (binding.make_config("cluster", cluster=8), 20, torch.bfloat16),
+    (binding.make_config("stream", cluster=7, grid_tokens=2), 31, torch.bfloat16),
+    (binding.make_config("stream", cluster=7, grid_tokens=2), 12, torch.float16),
+], ids=["cluster4", "cluster16", "pipe4", "cta", "deep-cluster8", "deep-stream7-walk",
+        "fp16-stream7-walk"])
+def test_exchange_wait_expires_and_reports(cfg, N, dtype):
+    inp = wl.make_inputs(5, N, H, seed=81, dtype=dtype).to("cuda")
     out = torch.empty_like(inp.prefix)
     newp = torch.empty_like(inp.prefix)
     binding.debug_exchange(extra_bytes=4, wait_ns=2_000_000)      # 2 ms
