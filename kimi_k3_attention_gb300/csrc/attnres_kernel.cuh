@@ -122,6 +122,24 @@ __device__ __forceinline__ float fma_rn(float a, float b, float c) {
   return r;
 }
 
+// Two float32 in one 64-bit register (lo in the low half), and the packed
+// fused multiply-add acc = a * b + acc on both halves, each rounded to
+// nearest even with subnormals kept.
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack_f32x2(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ void fma_rn_x2(unsigned long long& acc, unsigned long long a,
+                                          unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
 __device__ __forceinline__ float mul_rn(float a, float b) {
   float r;
   asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
@@ -690,11 +708,33 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
 #pragma unroll
       for (int e = 0; e < 8; ++e) h[k][e] = mul_rn(alpha[0], elem<DT>(u, e));
     }
+    if constexpr (VPT == 1) {
+      // the remaining sources with packed float32x2 FMAs (each lane an
+      // fma.rn.f32: the same bits as the scalar form, half the FMA
+      // instructions; GB300, M = 8192, N = 12: +2 % bandwidth)
+      unsigned long long h2[4];
 #pragma unroll
-    for (int i = 1; i < S; ++i) {
-      const uint4 u = src.get(i, k);
+      for (int q2 = 0; q2 < 4; ++q2) h2[q2] = pack_f32x2(h[k][2 * q2], h[k][2 * q2 + 1]);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) h[k][e] = fma_rn(alpha[i], elem<DT>(u, e), h[k][e]);
+      for (int i = 1; i < S; ++i) {
+        const uint4 u = src.get(i, k);
+        const unsigned long long a2 = pack_f32x2(alpha[i], alpha[i]);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2)
+          fma_rn_x2(h2[q2], a2, pack_f32x2(Fmt<DT>::lo(w4[q2]), Fmt<DT>::hi(w4[q2])));
+      }
+#pragma unroll
+      for (int q2 = 0; q2 < 4; ++q2) unpack_f32x2(h2[q2], h[k][2 * q2], h[k][2 * q2 + 1]);
+    } else {
+      // two chunks per thread: the packed form costs more registers than it
+      // saves instructions
+#pragma unroll
+      for (int i = 1; i < S; ++i) {
+        const uint4 u = src.get(i, k);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[k][e] = fma_rn(alpha[i], elem<DT>(u, e), h[k][e]);
+      }
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) q = fma_rn(h[k][e], h[k][e], q);
@@ -785,7 +825,9 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   if (p.prefetch & 2) griddep_launch_dependents();
   if (p.prefetch & 1) {
     const int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3) + 2;
-    for (int r = threadIdx.x; r < rows && cend > c0 && blockIdx.y < p.M; r += blockDim.x) {
+    // (a hint: with fewer threads than rows, the last rows go without)
+    if (static_cast<int>(threadIdx.x) < rows && cend > c0 && blockIdx.y < p.M) {
+      const int r = threadIdx.x;
       const size_t off = static_cast<size_t>(blockIdx.y) * p.H8 + c0;
       const uint32_t bytes = static_cast<uint32_t>(cend - c0) * 16u;
       const uint4* src = r < N ? p.bank + r * p.bank_stride + off
@@ -847,7 +889,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // and the next loads hit L2.
     if ((p.prefetch & 4) && m + static_cast<int>(gridDim.y) < p.M) {
       constexpr int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3);
-      for (int r = threadIdx.x; r < rows && cend > c0; r += blockDim.x) {
+      if (static_cast<int>(threadIdx.x) < rows && cend > c0) {
+        const int r = threadIdx.x;
         const size_t off = static_cast<size_t>(m + gridDim.y) * p.H8 + c0;
         const uint4* src = r < N ? p.bank + r * p.bank_stride + off
                          : r == N ? p.prefix + off
