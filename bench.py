@@ -11,9 +11,13 @@ host buffers, the clocks seen under load, and the CPU oracle's throughput.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Multi-GPU: one process per GPU (torchrun); each rank runs its own batch of
-8192 tokens (tokens are independent, no collective on the data path), so
-scaling is weak.
+Multi-GPU: one process per GPU; each rank runs its own batch of 8192 tokens
+(tokens are independent, no collective on the data path), so scaling is
+weak.  Under torchrun the ranks come from the environment; `--gpus N` with
+N > 1 outside torchrun starts the N ranks itself (torch.distributed.run on
+this node).  `--dry-run` runs the rank set-up, barriers, timing and
+max-over-ranks on the host only (gloo, no GPU, no kernel) to check that
+logic; its line says so and is not a measurement.
 """
 from __future__ import annotations
 
@@ -49,6 +53,25 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def free_port():
+    import socket
+    sk = socket.socket()
+    sk.bind(("127.0.0.1", 0))
+    port = sk.getsockname()[1]
+    sk.close()
+    return port
+
+
+def launch_ranks(argv, gpus):
+    """Start `gpus` ranks of this script on this node under
+    torch.distributed.run (rendezvous on 127.0.0.1) with the same arguments;
+    returns the launcher's exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={gpus}", "--master-addr", "127.0.0.1",
+           "--master-port", str(free_port()), os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd).returncode
 
 
 def rank_seed(rank):
@@ -196,6 +219,67 @@ def oracle_throughput(inp_cpu, budget_s, chunk=64, max_tokens=None):
             break
     bytes_ = algorithmic_bytes(done, inp_cpu.N, inp_cpu.H, inp_cpu.add2 is not None) - 4 * inp_cpu.H
     return bytes_ / el / 1e9, int(done), el, results
+
+
+def oracle_per_config(reps=3):
+    """The CPU oracle as it stands, on the host cores, per workload
+    configuration: the PR reference case (M=4, N=3), all 96 decode-sweep
+    cases, the bit-exactness stress case (M=32, N=12) and the 25-layer chain
+    (M=8, bank growing 1 -> 12), each in full; median of `reps` runs, one
+    thread.  Seconds per call (per chain for the chain) and GB/s of the
+    algorithmic bytes."""
+    import numpy as np
+    import torch
+    from kimi_k3_attention_gb300 import workloads as wl
+    from oracle import attnres_add_rmsnorm as oop
+
+    def u(t):
+        return None if t is None else t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    def args_of(inp):
+        return (u(inp.prefix), u(inp.add), u(inp.add2), u(inp.bank), u(inp.w), u(inp.gamma), inp.eps)
+
+    def med(fn):
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t0)
+        return statistics.median(ts)
+
+    def row(seconds, nbytes, **kw):
+        return dict(kw, s_per_call=round(seconds, 6), gbs=round(nbytes / seconds / 1e9, 4))
+
+    res = {}
+    pr = wl.pr_reference_case()
+    a = args_of(pr)
+    res["pr_reference_M4_N3"] = row(med(lambda: oop(*a)), algorithmic_bytes(4, 3, pr.H))
+    cases = [(M, N, ad, args_of(wl.decode_sweep_inputs(i, M, N, ad)))
+             for i, M, N, ad in wl.decode_sweep_cases()]
+    t = med(lambda: [oop(*c[3]) for c in cases])
+    nb = sum(algorithmic_bytes(M, N, H, ad) for M, N, ad, _ in cases)
+    res["decode_sweep_96_cases"] = row(t / len(cases), nb / len(cases), cases=len(cases),
+                                       s_all_cases=round(t, 4))
+    st = wl.stress_inputs(special_prefix=True)
+    a = args_of(st)
+    res["stress_M32_N12"] = row(med(lambda: oop(*a)), algorithmic_bytes(32, 12, H))
+    emb, p0, layers = wl.chain_inputs(M=8, H=H, layers=25)
+
+    def chain():
+        bank, P = [u(emb)], u(p0)
+        for li, L in enumerate(layers):
+            P, _, _ = oop(P, u(L.routed), u(L.shared), np.stack(bank), u(L.w), u(L.gamma), wl.EPS)
+            if wl.chain_appends_after(li):
+                bank.append(P.copy())
+    nb, n = 0, 1
+    for li in range(25):
+        nb += algorithmic_bytes(8, n, H)
+        n += 1 if wl.chain_appends_after(li) else 0
+    res["chain_25_layers_M8"] = row(med(chain), nb, unit_of_s="per 25-layer chain")
+    model, ncpu = cpu_info()
+    res.update(threads=1, reps=reps, cpu=model, host_cpus=ncpu,
+               note="reported baseline, not a target")
+    return res
 
 
 def cpu_info():
@@ -675,7 +759,8 @@ def run_ours(args):
         model, ncpu = cpu_info()
         cpu_base = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                     "sample": f"first {done} of the 8192 tokens, {el:.1f} s",
-                    "cpu": model, "host_cpus": ncpu, "gpu_outputs_match_on_sample": parity}
+                    "cpu": model, "host_cpus": ncpu, "gpu_outputs_match_on_sample": parity,
+                    "per_config": oracle_per_config()}
 
     if rank != 0:
         if ws > 1:
@@ -721,9 +806,49 @@ def run_ours(args):
     return 0
 
 
+def run_dry(args):
+    """The multi-rank host logic alone: process group (gloo), barriers around
+    K timed host steps (rank r sleeps (r + 1) ms, so the slowest rank is
+    known), max over ranks, one line from rank 0.  No GPU, no kernel."""
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        dist.init_process_group("gloo")
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        time.sleep(0.001 * (rank + 1))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time.sleep(0.001 * (rank + 1))
+    el = time.perf_counter() - t0
+    barrier()
+    total_s = max_over_ranks(el, "cpu")
+    if rank == 0:
+        nbytes = algorithmic_bytes(M_BW, N_BW, H)
+        print(json.dumps({"metric": METRIC, "dry_run": True, "n_gpus": ws, "steps": args.steps,
+                          "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 4),
+                          "value": round(weak_scaling_value(nbytes, ws, args.steps, total_s), 4),
+                          "unit": UNIT, "scaling": "weak",
+                          "note": "host logic only (gloo ranks sleeping, no GPU): not a measurement"}),
+              flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=None,
+                    help="GPUs (ranks) of this node; default 1, or WORLD_SIZE under torchrun")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="host-side multi-rank logic only (gloo, no GPU); not a measurement")
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
@@ -746,6 +871,16 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    env_ws = os.environ.get("WORLD_SIZE")
+    if env_ws is None:
+        if args.gpus is not None and args.gpus > 1:
+            # not under a launcher: start the ranks here, one per GPU
+            return launch_ranks(argv, args.gpus)
+    elif args.gpus is not None and args.gpus != int(env_ws):
+        sys.stderr.write(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={env_ws}\n")
+        return 2
+    if args.dry_run:
+        return run_dry(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -9,7 +9,10 @@
  *        new_prefix = bf16(prefix + s)
  *      Both additions are float32 round-to-nearest-even with subnormals kept
  *      (no flush to zero); each result is rounded to BF16 to nearest even.
- *      This is bit for bit the result of the two BF16 tensor additions.
+ *      This is bit for bit the result of the two BF16 tensor additions, and
+ *      bit for bit the exact sum rounded once to BF16 (float32 holds the
+ *      sum of two BF16 values closely enough that the second rounding never
+ *      differs), which is how the kernels compute it.
  *      Defined in: TensorRT-LLM PR #20546 ("Kimi K3: fold the MoE-tail
  *      additions into the next attention-residual"), section "Op", the
  *      optional trailing layer_residual_add2 of attn_res_add_rmsnorm_fwd.
@@ -39,6 +42,16 @@
  *     launches nothing and returns a negative status.  A failed launch returns
  *     ATTNRES_ERR_CUDA and attnres_last_cuda_error() holds the cudaError_t.
  *     No entry point aborts, traps or prints.
+ *   - A failure inside a running kernel cannot be returned by the call (it
+ *     is asynchronous).  The one the kernels detect is a CTA of a cluster
+ *     waiting longer than a time limit (200 ms) for its peers' partial
+ *     sums, which happens only if the GPU does not run the CTAs of a cluster
+ *     together.  The kernel then finishes without hanging, writes NaN into
+ *     every element of out (and h_out) that depended on the exchange
+ *     (new_prefix does not, and stays exact), and sets a bit that
+ *     attnres_device_status() reports.  A caller that must not consume such
+ *     outputs checks that status word after synchronising, or tests out for
+ *     NaN.
  *   - Aliasing: new_prefix may be exactly prefix (in-place carry-on of the
  *     prefix sum) or any region that overlaps no input (e.g. bank slot N,
  *     which the call does not read).  out may overlap nothing.
@@ -120,7 +133,12 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *                 exchanged through distributed shared memory;
  *             3 = as 2 with at most 224 threads and registers capped so that
  *                 three CTAs share an SM;
- *             Variants 1 and 4 exist for N <= 12 only.  For N > 12
+ *             5 = as 2 with registers capped so that two CTAs of up to 256
+ *                 threads share an SM (in back-to-back calls the next
+ *                 call's CTAs can become resident, and prefetch, while this
+ *                 call runs);
+ *             Variants 1, 4 and 5 exist for N <= 12 only (variant 5 with
+ *             the fold on BF16 tensors only).  For N > 12
  *             variant 3 takes at most 128 threads, registers capped so
  *             that four or five CTAs share an SM (from N = 23 on with
  *             bank rows 16..N-1 in dynamic shared memory).
@@ -131,7 +149,7 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *                 so HBM reads continue during the reductions.
  *             All variants give bit-identical new_prefix; out is identical
  *             for the same variant family and cluster size.
- *   cluster   CTAs per token for variants 2 and 3 (1..16); 0 = the
+ *   cluster   CTAs per token for variants 2, 3 and 5 (1..16); 0 = the
  *             smallest that fits the variant's thread limit.
  *   threads   threads per CTA, a multiple of 32 within the variant's limit;
  *             0 = the smallest count that covers the CTA's columns.
@@ -146,7 +164,7 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *   stages    variant 4 only: tokens held by the shared-memory ring (2..4);
  *             0 = as many as fit 227 KB of shared memory.  Must be 0 for
  *             the other variants.
- *   prefetch  variants 2 and 3, a bit mask: 1 = before waiting on the
+ *   prefetch  variants 2, 3 and 5, a bit mask: 1 = before waiting on the
  *             previous kernel (see pdl), ask L2 to fetch this CTA's rows of
  *             its first token; 2 = let the next kernel be scheduled at once;
  *             4 = while a token is reduced, ask L2 for the CTA's rows of the
@@ -224,6 +242,16 @@ int attnres_rmsnorm(const void* prefix, const void* bank, const void* w,
 int attnres_tail_add(const void* prefix, const void* add, const void* add2,
                      void* new_prefix, int M, int H, attnres_stream_t stream);
 
+/*
+ * attnres_tail_add_f16 -- attnres_tail_add on FP16 tensors:
+ * new_prefix = fp16(prefix + fp16(add + add2)), each addition the exact sum
+ * rounded once to FP16 (nearest even, subnormals kept, overflow to
+ * infinity), which is bit for bit the float32 addition rounded to FP16.  The
+ * comparator of attnres_add_rmsnorm_f16.  Same arguments and aliasing rules.
+ */
+int attnres_tail_add_f16(const void* prefix, const void* add, const void* add2,
+                         void* new_prefix, int M, int H, attnres_stream_t stream);
+
 /* All arguments of one call, for attnres_launch. */
 typedef struct {
   const void* prefix;
@@ -241,9 +269,9 @@ typedef struct {
   int dtype;              /* ATTNRES_DTYPE_BF16 or ATTNRES_DTYPE_FP16       */
 } attnres_args;
 
-/* Any of the calls above (tail_add excepted) with a pinned configuration
- * (cfg may be NULL).  The attention-residual alone (fold = 0) and FP16
- * tensors exist for variants 2 and 3 only; other variants return
+/* Any of the calls above (the tail adds excepted) with a pinned
+ * configuration (cfg may be NULL).  The attention-residual alone (fold = 0)
+ * and FP16 tensors exist for variants 2 and 3 only; other variants return
  * ATTNRES_ERR_CONFIG. */
 int attnres_launch(const attnres_args* args, const attnres_config* cfg,
                    attnres_stream_t stream);
@@ -264,8 +292,8 @@ int attnres_last_cuda_error(void);
 
 /* Status word the kernels of the current device write, for failures they
  * cannot return: bit 0 (ATTNRES_DEVICE_WAIT_TIMEOUT) is set when a CTA of a
- * cluster waited longer than the limit for its peers' partial sums (the
- * call's outputs are then wrong).  Reads it into *bits (and zeroes it when
+ * cluster waited longer than the limit for its peers' partial sums (that
+ * call wrote NaN into the outputs that depended on them).  Reads it into *bits (and zeroes it when
  * `clear` is non-zero).  Synchronous: waits for the device's work to finish.
  * No correct call sets a bit. */
 #define ATTNRES_DEVICE_WAIT_TIMEOUT 1u

@@ -21,7 +21,7 @@ STATUS = {
 }
 DTYPE_BF16, DTYPE_FP16 = 0, 1
 ATTNRES_DEVICE_WAIT_TIMEOUT = 1
-VARIANTS = {"auto": 0, "cta": 1, "cluster": 2, "stream": 3, "pipe": 4}
+VARIANTS = {"auto": 0, "cta": 1, "cluster": 2, "stream": 3, "pipe": 4, "cluster2": 5}
 
 # Every symbol include/attnres.h declares.
 EXPORTS = (
@@ -31,6 +31,7 @@ EXPORTS = (
     "attnres_add_rmsnorm_f16",
     "attnres_rmsnorm",
     "attnres_tail_add",
+    "attnres_tail_add_f16",
     "attnres_launch",
     "attnres_plan",
     "attnres_status_string",
@@ -98,6 +99,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attnres_rmsnorm.restype = i
     lib.attnres_tail_add.argtypes = [vp, vp, vp, vp, i, i, vp]
     lib.attnres_tail_add.restype = i
+    lib.attnres_tail_add_f16.argtypes = [vp, vp, vp, vp, i, i, vp]
+    lib.attnres_tail_add_f16.restype = i
     lib.attnres_launch.argtypes = [ctypes.POINTER(Args), ctypes.POINTER(Config), vp]
     lib.attnres_launch.restype = i
     lib.attnres_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
@@ -239,14 +242,18 @@ def attnres_rmsnorm(prefix, bank, w, gamma, eps, out, stream=None, config: Optio
 
 
 def attnres_tail_add(prefix, add, add2, new_prefix, stream=None):
-    """The standalone fold: new_prefix = bf16(prefix + bf16(add + add2))."""
+    """The standalone fold: new_prefix = bf16(prefix + bf16(add + add2))
+    (fp16(prefix + fp16(add + add2)) for float16 tensors)."""
     M, H = prefix.shape
+    dt = prefix.dtype
+    code = _dtype_code(prefix)
     for name, t in (("prefix", prefix), ("add", add), ("new_prefix", new_prefix)):
-        _check_tensor(name, t, (M, H))
+        _check_tensor(name, t, (M, H), dt)
     if add2 is not None:
-        _check_tensor("add2", add2, (M, H))
-    _check(load().attnres_tail_add(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(new_prefix), M, H,
-                                   _stream_handle(stream)))
+        _check_tensor("add2", add2, (M, H), dt)
+    lib = load()
+    fn = lib.attnres_tail_add_f16 if code == DTYPE_FP16 else lib.attnres_tail_add
+    _check(fn(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(new_prefix), M, H, _stream_handle(stream)))
 
 
 def launch(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, h_out=None, M=None, N=None,

@@ -209,6 +209,7 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
       c->cluster = cl < lo ? lo : (cl > 16 ? 16 : cl);
     }
   }
+  if (deep && c->variant == 5) return ATTNRES_ERR_CONFIG;
   if (c->variant == 1) {
     if (c->cluster == 0) c->cluster = 1;
     if (c->cluster != 1) return ATTNRES_ERR_CONFIG;
@@ -216,8 +217,8 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
     if (c->threads == 0) c->threads = need;
     if (c->threads < need || c->threads > kCtaMaxT || (c->threads % 32) != 0)
       return ATTNRES_ERR_CONFIG;
-  } else if (c->variant == 2 || c->variant == 3) {
-    const int maxt = (c->variant == 2) ? kSplitMaxT : stream_maxt;
+  } else if (c->variant == 2 || c->variant == 3 || c->variant == 5) {
+    const int maxt = (c->variant == 3) ? stream_maxt : kSplitMaxT;
     if (c->cluster == 0) c->cluster = min_cluster(maxt);
     if (c->cluster < 1 || c->cluster > 16) return ATTNRES_ERR_CONFIG;
     const int cpc = (H8 + c->cluster - 1) / c->cluster;
@@ -275,12 +276,13 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
   if (c->pdl == 0) c->pdl = 1;
   if (c->prefetch < -1 || c->prefetch > 7) return ATTNRES_ERR_CONFIG;
   if (c->prefetch == 0) {
-    const bool fused = c->variant == 2 || c->variant == 3;
+    const bool fused = c->variant == 2 || c->variant == 3 || c->variant == 5;
     c->prefetch = (fused && M <= 96) ? 1 : 0;
     if (fused && c->grid_tokens < M) c->prefetch |= 4;   // clusters walk tokens
     if (c->prefetch == 0) c->prefetch = -1;
   }
-  if (c->prefetch > 0 && c->variant != 2 && c->variant != 3) return ATTNRES_ERR_CONFIG;
+  if (c->prefetch > 0 && c->variant != 2 && c->variant != 3 && c->variant != 5)
+    return ATTNRES_ERR_CONFIG;
   return ATTNRES_OK;
 }
 
@@ -461,6 +463,9 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   else if (c.variant == 2)
     e = dispatch<kSplitVPT, kSplitMaxT, kSplitMinB>(a.N, has_add2, p, grid, c.threads, c.cluster,
                                                     pdl, s);
+  else if (c.variant == 5)
+    e = dispatch<kSplitVPT, kSplitMaxT, kSplit2MinB>(a.N, has_add2, p, grid, c.threads, c.cluster,
+                                                     pdl, s);
   else if (c.variant == 3)
     e = dispatch<kStreamVPT, kStreamMaxT, kStreamMinB>(a.N, has_add2, p, grid, c.threads,
                                                        c.cluster, pdl, s);
@@ -551,8 +556,11 @@ extern "C" int attnres_launch(const attnres_args* args, const attnres_config* cf
              cfg, reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" int attnres_tail_add(const void* prefix, const void* add, const void* add2,
-                                void* new_prefix, int M, int H, attnres_stream_t stream) {
+namespace attnres {
+namespace {
+
+int tail_add(const void* prefix, const void* add, const void* add2, void* new_prefix, int M,
+             int H, int dtype, attnres_stream_t stream) {
   if (!prefix || !add || !new_prefix) return ATTNRES_ERR_NULL;
   if (M < 1 || H < 8 || H > ATTNRES_MAX_H || (H % 8) != 0) return ATTNRES_ERR_SHAPE;
   if (misaligned(prefix) || misaligned(add) || (add2 && misaligned(add2)) || misaligned(new_prefix))
@@ -570,10 +578,28 @@ extern "C" int attnres_tail_add(const void* prefix, const void* add, const void*
   const uint4* a4 = static_cast<const uint4*>(add);
   const uint4* b4 = static_cast<const uint4*>(add2);
   uint4* n4 = static_cast<uint4*>(new_prefix);
-  cudaError_t e = add2 ? launch_tail_add<true>(p4, a4, b4, n4, chunks, sms, true, s)
-                       : launch_tail_add<false>(p4, a4, b4, n4, chunks, sms, true, s);
+  cudaError_t e;
+  if (dtype == ATTNRES_DTYPE_FP16)
+    e = add2 ? launch_tail_add<true, kFP16>(p4, a4, b4, n4, chunks, sms, true, s)
+             : launch_tail_add<false, kFP16>(p4, a4, b4, n4, chunks, sms, true, s);
+  else
+    e = add2 ? launch_tail_add<true, kBF16>(p4, a4, b4, n4, chunks, sms, true, s)
+             : launch_tail_add<false, kBF16>(p4, a4, b4, n4, chunks, sms, true, s);
   if (e != cudaSuccess) return fail_cuda(e);
   return ATTNRES_OK;
+}
+
+}  // namespace
+}  // namespace attnres
+
+extern "C" int attnres_tail_add(const void* prefix, const void* add, const void* add2,
+                                void* new_prefix, int M, int H, attnres_stream_t stream) {
+  return tail_add(prefix, add, add2, new_prefix, M, H, ATTNRES_DTYPE_BF16, stream);
+}
+
+extern "C" int attnres_tail_add_f16(const void* prefix, const void* add, const void* add2,
+                                    void* new_prefix, int M, int H, attnres_stream_t stream) {
+  return tail_add(prefix, add, add2, new_prefix, M, H, ATTNRES_DTYPE_FP16, stream);
 }
 
 extern "C" int attnres_plan(int M, int N, int H, int has_add2, attnres_config* plan) {

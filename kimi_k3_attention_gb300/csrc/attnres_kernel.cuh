@@ -11,10 +11,12 @@
 //           reduces the current one), or cp.async copies into a per-thread
 //           shared-memory ring several tokens ahead (attnres_pipe_kernel,
 //           persistent)
-//   fold    new_prefix = bf16(prefix + bf16(add + add2)) with add.rn.f32 and
-//           cvt.rn.bf16x2.f32 written in PTX, so no fast-math flag can turn
-//           them into flush-to-zero forms (TensorRT-LLM PR #20546, "Op");
-//           FP16 tensors round to FP16 instead (Fmt<kFP16>)
+//   fold    new_prefix = bf16(prefix + bf16(add + add2)), each addition
+//           the exact sum rounded once to BF16: the bits of the float32
+//           round-to-nearest additions of TensorRT-LLM PR #20546 ("Op"),
+//           written as paired BF16 additions in PTX (add.rn.bf16x2, which
+//           has no flush-to-zero form, so no fast-math flag can flush
+//           subnormal sums); FP16 tensors round to FP16 (Fmt<kFP16>)
 //   stats   ss_i = sum v^2 and d_i = w.v for the N+1 sources, one pass of
 //           mixed-precision FMAs (16-bit operands, float32 accumulators)
 //   R1      2(N+1) partial sums: warp transpose-reduction (one per group of
@@ -35,8 +37,9 @@
 // every CTA reaches both on the same path), cp.async.wait_group (completes
 // with its copies), griddepcontrol.wait (completes with the previous grid),
 // and the exchange mbarriers, whose waits are bounded in time: on expiry the
-// kernel sets a bit in the library's status word, stops waiting, and stays
-// resident for the same bound before exiting.
+// kernel sets a bit in the library's status word, stops waiting, writes NaN
+// in place of the outputs that depend on the exchange, and stays resident
+// for the same bound before exiting.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -83,19 +86,38 @@ constexpr unsigned FULL = 0xffffffffu;
 
 // ---------------------------------------------------------------- PTX helpers
 
+// Global loads.  Each is volatile with a memory clobber, so the compiler
+// keeps it after griddep_wait(): under programmatic dependent launch the
+// data may be written by the previous kernel on the stream.
+//   ld_stream: read once, not kept in L1, through the non-coherent path;
+//              only for tensors no thread of the kernel writes
+//   ld_prefix: read once, not kept in L1, coherent; for the prefix sum,
+//              which the call may overwrite in place with the new prefix
+//   ld_keep:   small read-only vectors (w, gamma), cached
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_prefix(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
   return r;
 }
 
 __device__ __forceinline__ uint4 ld_keep(const uint4* p) {
   uint4 r;
-  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
   return r;
 }
 
@@ -103,13 +125,6 @@ __device__ __forceinline__ void st_out(uint4* p, const uint4& v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
-}
-
-// float32 addition, round to nearest even, subnormals kept (no .ftz).
-__device__ __forceinline__ float add_rn(float a, float b) {
-  float r;
-  asm("add.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-  return r;
 }
 
 // float32 fused multiply-add and multiply, round to nearest even, subnormal
@@ -162,6 +177,7 @@ struct Fmt;
 
 template <>
 struct Fmt<kBF16> {
+  static constexpr uint32_t kNaN2 = 0x7FC07FC0u;   // a quiet NaN in both lanes
   // integer moves only
   static __device__ __forceinline__ float lo(uint32_t u) { return __uint_as_float(u << 16); }
   static __device__ __forceinline__ float hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
@@ -177,10 +193,18 @@ struct Fmt<kBF16> {
         : "+f"(ss), "+f"(d)
         : "r"(x), "r"(w));
   }
+  // a + b on both lanes, the exact sum rounded once to BF16 (nearest even,
+  // subnormals kept)
+  static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+  }
 };
 
 template <>
 struct Fmt<kFP16> {
+  static constexpr uint32_t kNaN2 = 0x7E007E00u;   // a quiet NaN in both lanes
   // FP16 subnormals are normal float32 values: the conversion is exact
   static __device__ __forceinline__ float lo(uint32_t u) {
     float r;
@@ -204,6 +228,13 @@ struct Fmt<kFP16> {
         : "+f"(ss), "+f"(d)
         : "r"(x), "r"(w));
   }
+  // a + b on both lanes, the exact sum rounded once to FP16 (nearest even,
+  // subnormals kept: no .ftz)
+  static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+  }
 };
 
 // Element e (0..7) of a 16-byte chunk as float32.
@@ -213,14 +244,19 @@ __device__ __forceinline__ float elem(const uint4& v, int e) {
   return (e & 1) ? Fmt<DT>::hi(u) : Fmt<DT>::lo(u);
 }
 
-// One 32-bit word (two lanes) of the fold: float32 additions, each result
-// rounded to the element format.
+// One 32-bit word (two lanes) of the fold.  The pages' arithmetic is a
+// float32 round-to-nearest addition rounded to the element format (BF16 or
+// FP16).  The sum of two 16-bit values is exact in float32 unless it
+// overflows or needs more than 24 significant bits, and rounding a float32
+// result to a format of p <= 11 bits gives the correctly rounded sum
+// whenever 24 >= 2p + 2 (double rounding is innocuous).  So the paired
+// 16-bit addition, which rounds the exact sum once, gives the same bits
+// (subnormals and signed zeros included) in one instruction per pair.
 template <bool ADD2, int DT>
 __device__ __forceinline__ uint32_t fold_word(uint32_t p, uint32_t a, uint32_t a2) {
   using F = Fmt<DT>;
-  uint32_t s = a;
-  if (ADD2) s = F::pack(add_rn(F::lo(a), F::lo(a2)), add_rn(F::hi(a), F::hi(a2)));
-  return F::pack(add_rn(F::lo(p), F::lo(s)), add_rn(F::hi(p), F::hi(s)));
+  const uint32_t s = ADD2 ? F::add(a, a2) : a;
+  return F::add(p, s);
 }
 
 template <bool ADD2, int DT>
@@ -755,7 +791,10 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
   qq = warp_sum(qq);
   const float rh = rsqrtf(__fmaf_rn(qq, p.inv_h, p.eps));
 
-  // ---- outputs
+  // ---- outputs (after a timed-out exchange wait the sums are partial: out
+  // and h_out are written as NaN, so that no wrong value passes as a
+  // result; new_prefix does not depend on the exchange and stays exact)
+  const uint4 nan4 = make_uint4(Fmt<DT>::kNaN2, Fmt<DT>::kNaN2, Fmt<DT>::kNaN2, Fmt<DT>::kNaN2);
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     if (ok[k]) {
@@ -766,7 +805,7 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
         hv.y = Fmt<DT>::pack(h[k][2], h[k][3]);
         hv.z = Fmt<DT>::pack(h[k][4], h[k][5]);
         hv.w = Fmt<DT>::pack(h[k][6], h[k][7]);
-        st_out(p.h_out + row + jj[k], hv);
+        st_out(p.h_out + row + jj[k], t.failed ? nan4 : hv);
       }
       uint4 o;
       o.x = Fmt<DT>::pack(mul_rn(mul_rn(h[k][0], rh), elem<DT>(gv[k], 0)),
@@ -777,7 +816,7 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
                           mul_rn(mul_rn(h[k][5], rh), elem<DT>(gv[k], 5)));
       o.w = Fmt<DT>::pack(mul_rn(mul_rn(h[k][6], rh), elem<DT>(gv[k], 6)),
                           mul_rn(mul_rn(h[k][7], rh), elem<DT>(gv[k], 7)));
-      st_out(p.out + row + jj[k], o);
+      st_out(p.out + row + jj[k], t.failed ? nan4 : o);
     }
   }
 }
@@ -867,7 +906,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const uint4 z = make_uint4(0, 0, 0, 0);
-      pr[k] = ok[k] ? ld_stream(p.prefix + row + jj[k]) : z;
+      pr[k] = ok[k] ? ld_prefix(p.prefix + row + jj[k]) : z;
       ad[k] = (MODE != kNoFold && ok[k]) ? ld_stream(p.add + row + jj[k]) : z;
       ad2[k] = (MODE == kFoldAdd2 && ok[k]) ? ld_stream(p.add2 + row + jj[k]) : z;
 #pragma unroll
@@ -997,18 +1036,20 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
 // The standalone fold: new_prefix = bf16(prefix + bf16(add + add2)) (or
 // bf16(prefix + add)) over n 16-byte chunks, grid-stride, 16-byte vectors.
 // The addition that the fused kernel replaces; kept for comparison.
-template <bool ADD2>
-__global__ void __launch_bounds__(256) attnres_tail_add_kernel(const uint4* __restrict__ prefix,
+// new_prefix may be prefix itself (in place): prefix is read with a
+// coherent load, and neither pointer is marked restrict.
+template <bool ADD2, int DT>
+__global__ void __launch_bounds__(256) attnres_tail_add_kernel(const uint4* prefix,
                                                                const uint4* __restrict__ add,
                                                                const uint4* __restrict__ add2,
-                                                               uint4* __restrict__ new_prefix,
+                                                               uint4* new_prefix,
                                                                long long n) {
   griddep_wait();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += stride) {
     const uint4 a2 = ADD2 ? ld_stream(add2 + i) : make_uint4(0, 0, 0, 0);
-    st_out(new_prefix + i, fold_chunk<ADD2, kBF16>(ld_stream(prefix + i), ld_stream(add + i), a2));
+    st_out(new_prefix + i, fold_chunk<ADD2, DT>(ld_prefix(prefix + i), ld_stream(add + i), a2));
   }
   griddep_launch_dependents();
 }
@@ -1020,7 +1061,7 @@ cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, b
 template <int N, bool ADD2, int STAGES>
 cudaError_t launch_pipe(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
                         cudaStream_t s);
-template <bool ADD2>
+template <bool ADD2, int DT>
 cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* add2,
                             uint4* new_prefix, long long chunks, int sms, bool pdl,
                             cudaStream_t s);

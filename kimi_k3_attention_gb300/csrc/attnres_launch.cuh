@@ -17,6 +17,10 @@ constexpr int kMaxDevices = 64;
 //           deep banks have their own streaming shape (below)
 //   cta:    16 columns per thread, up to 448 threads (one CTA per token)
 constexpr int kSplitVPT = 1, kSplitMaxT = 256, kSplitMinB = 1;
+// split2: the split shape with registers capped so that two CTAs of up to
+// 256 threads share an SM (the next call's CTAs can be resident while this
+// call runs, under programmatic dependent launch)
+constexpr int kSplit2MinB = 2;
 constexpr int kStreamVPT = 1, kStreamMaxT = 224, kStreamMinB = 3;
 constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 
@@ -150,7 +154,7 @@ cudaError_t launch_pipe(const Params& p, dim3 grid, int threads, int cluster, bo
 
 // The standalone fold over M*H/8 chunks: 256-thread CTAs, at most 8 per SM
 // worth of grid (grid-stride beyond that).
-template <bool ADD2>
+template <bool ADD2, int DT>
 cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* add2,
                             uint4* new_prefix, long long chunks, int sms, bool pdl,
                             cudaStream_t s) {
@@ -165,7 +169,7 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attnres_tail_add_kernel<ADD2>, prefix, add, add2, new_prefix,
+  return cudaLaunchKernelEx(&cfg, attnres_tail_add_kernel<ADD2, DT>, prefix, add, add2, new_prefix,
                             chunks);
 }
 
@@ -192,6 +196,7 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
 // N <= 12 with the fold (add2 present or not): every shape.
 #define ATTNRES_INSTANTIATE(DEF, N, ADD2)                                                   \
   ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB)     \
+  ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kSplitVPT, kSplitMaxT, kSplit2MinB)    \
   ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kStreamVPT, kStreamMaxT, kStreamMinB)  \
   ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kCtaVPT, kCtaMaxT, kCtaMinB)           \
   ATTNRES_PIPE(DEF, N, ADD2, 2)                                                             \
@@ -226,11 +231,12 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   ATTNRES_FUSED_DT(DEF, N, kFoldAdd, kStreamVPT, kStreamMaxT, kStreamMinB, kFP16)      \
   ATTNRES_FUSED_DT(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, kStreamMinB, kFP16)
 
-#define ATTNRES_INSTANTIATE_TAIL_ADD(DEF)                                                  \
-  DEF template cudaError_t launch_tail_add<true>(const uint4*, const uint4*, const uint4*,  \
-                                                 uint4*, long long, int, bool, cudaStream_t); \
-  DEF template cudaError_t launch_tail_add<false>(const uint4*, const uint4*, const uint4*, \
-                                                  uint4*, long long, int, bool, cudaStream_t);
+#define ATTNRES_TAIL_ADD(DEF, ADD2, DT)                                                      \
+  DEF template cudaError_t launch_tail_add<ADD2, DT>(const uint4*, const uint4*, const uint4*,  \
+                                                     uint4*, long long, int, bool, cudaStream_t);
+#define ATTNRES_INSTANTIATE_TAIL_ADD(DEF)                                    \
+  ATTNRES_TAIL_ADD(DEF, true, kBF16) ATTNRES_TAIL_ADD(DEF, false, kBF16)     \
+  ATTNRES_TAIL_ADD(DEF, true, kFP16) ATTNRES_TAIL_ADD(DEF, false, kFP16)
 
 // Which unit defines what.
 #define ATTNRES_UNIT_A(DEF)                                                             \

@@ -73,7 +73,8 @@ def _ceil(a, b):
 
 def split_configs(H):
     """Every cluster size whose CTAs fit the split shape (<= 256 threads of 8
-    columns), the register-capped shape (<= 224 threads) or the pipelined
+    columns; registers uncapped, or capped for two CTAs per SM), the
+    register-capped streaming shape (<= 224 threads) or the pipelined
     persistent kernel (<= 256 threads) for this H, the one-CTA-per-token
     variant where it fits (<= 448 threads of 16 columns), and the automatic
     choice (None)."""
@@ -82,6 +83,9 @@ def split_configs(H):
     for c in range(1, 17):
         if _ceil(_ceil(H8, c), 32) * 32 <= 256:
             cfgs.append(binding.make_config("cluster", cluster=c))
+    for c in range(1, 17):
+        if _ceil(_ceil(H8, c), 32) * 32 <= 256:
+            cfgs.append(binding.make_config("cluster2", cluster=c))
     for c in range(1, 17):
         if _ceil(_ceil(H8, c), 32) * 32 <= 224:
             cfgs.append(binding.make_config("stream", cluster=c))
@@ -99,6 +103,6 @@ def cfg_name(c):
     d = c.as_dict()
     if d["variant"] == 1:
         return "cta"
-    name = {2: "cluster", 3: "stream", 4: "pipe"}[d["variant"]]
+    name = {2: "cluster", 3: "stream", 4: "pipe", 5: "cluster2"}[d["variant"]]
     extra = f"s{d['stages']}" if d["stages"] else ""
     return f"{name}{d['cluster']}{extra}"

@@ -61,3 +61,29 @@ def test_reference_arm_prints_on_rank0_only():
                         "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True,
                        timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_gpus_flag_starts_the_ranks_itself():
+    """`bench.py --gpus 2` outside a launcher starts two ranks on this node
+    (torch.distributed.run); the dry run exercises the rank set-up, barriers,
+    timing and max over ranks with gloo and no GPU: exactly one line, from
+    rank 0, with n_gpus 2 and the slower rank's time."""
+    import json
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--dry-run", "--gpus", "2",
+                        "--steps", "5", "--warmup", "3"], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["dry_run"] and d["scaling"] == "weak"
+    assert d["ms_per_step"] >= 2.0          # rank 1 sleeps 2 ms per step
+
+
+def test_gpus_flag_must_match_the_launcher():
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--dry-run", "--gpus", "4",
+                        "--steps", "1"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2 and "WORLD_SIZE" in r.stderr
