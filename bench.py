@@ -358,9 +358,10 @@ def time_bandwidth(binding, inp, steps, warmup, stream, config=None):
     return call, ev, t_all0, t_all1, out, newp
 
 
-def decode_latencies(binding, wl, reps=200, replays=20):
-    """Microseconds per call in the decode window (H=7168, both addends), from
-    CUDA-graph replays of back-to-back calls on one stream:
+def _decode_shape_times(binding, M, N, configs, seed, reps=200, replays=20):
+    """Microseconds per call at (M, N), H=7168, both addends, for each named
+    launch configuration (None = the library's choice), from CUDA-graph
+    replays of back-to-back calls on one stream:
       warm: `reps` calls on the same buffers (inputs L2-resident);
       cold: calls cycling through distinct buffer sets whose total exceeds
             2.5x the L2 size, so every call reads its inputs from HBM.
@@ -368,61 +369,119 @@ def decode_latencies(binding, wl, reps=200, replays=20):
     import torch
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or (128 << 20)
     s = torch.cuda.Stream()
+    per_set = algorithmic_bytes(M, N, H)
+    nsets = max(2, min(4096, -(-int(2.5 * l2) // per_set)))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    rnd = lambda *shape: torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)  # noqa: E731
+    P, A, A2 = rnd(nsets, M, H), rnd(nsets, M, H), rnd(nsets, M, H)
+    B = rnd(nsets, N, M, H)
+    w = (rnd(H).float() / H ** 0.5).to(torch.bfloat16)
+    gam = (1 + 0.1 * rnd(H).float()).to(torch.bfloat16)
+    O = torch.empty_like(P)
+    NP = torch.empty_like(P)
+
+    def timed(graph, calls):
+        out = []
+        for _ in range(replays):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                e0.record(s)
+                graph.replay()
+                e1.record(s)
+            e1.synchronize()
+            out.append(e0.elapsed_time(e1) * 1e3 / calls)
+        return round(statistics.median(out), 3)
+
+    res = {}
+    for name, cfg in configs.items():
+        def call(i, cfg=cfg):
+            binding.attnres_add_rmsnorm(P[i], A[i], A2[i], B[i], w, gam, 1e-6, O[i], NP[i],
+                                        stream=s, check=False, config=cfg)
+        with torch.cuda.stream(s):
+            for i in range(min(nsets, 8)):
+                call(i)
+        torch.cuda.synchronize()
+        gw = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gw, stream=s):
+            for _ in range(reps):
+                call(0)
+        gc = torch.cuda.CUDAGraph()
+        ncold = max(reps, nsets)
+        with torch.cuda.graph(gc, stream=s):
+            for k in range(ncold):
+                call(k % nsets)
+        with torch.cuda.stream(s):
+            gw.replay()
+            gc.replay()
+        torch.cuda.synchronize()
+        res[name] = {"warm_us": timed(gw, reps), "cold_us": timed(gc, ncold), "cold_sets": nsets,
+                     "plan": binding.attnres_plan(M, N, H) if cfg is None else cfg.as_dict()}
+        del gw, gc
+    del P, A, A2, B, O, NP
+    torch.cuda.synchronize()
+    return res
+
+
+def decode_latencies(binding, wl):
+    """The decode window (M <= 32 tokens), automatic launch configuration:
+    warm and cold microseconds per call (see _decode_shape_times)."""
     res = {}
     for M in (1, 8, 16, 32):
         for N in (1, 3, 6, 12):
-            per_set = algorithmic_bytes(M, N, H)
-            nsets = max(2, min(4096, -(-int(2.5 * l2) // per_set)))
-            g = torch.Generator(device="cuda")
-            g.manual_seed(900 + M * 16 + N)
-            rnd = lambda *shape: torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)  # noqa: E731
-            P, A, A2 = rnd(nsets, M, H), rnd(nsets, M, H), rnd(nsets, M, H)
-            B = rnd(nsets, N, M, H)
-            w = (rnd(H) / H ** 0.5).to(torch.bfloat16)
-            gam = (1 + 0.1 * rnd(H).float()).to(torch.bfloat16)
-            O = torch.empty_like(P)
-            NP = torch.empty_like(P)
-
-            def call(i):
-                binding.attnres_add_rmsnorm(P[i], A[i], A2[i], B[i], w, gam, 1e-6, O[i], NP[i],
-                                            stream=s, check=False)
-
-            def timed(graph, calls):
-                out = []
-                for _ in range(replays):
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    with torch.cuda.stream(s):
-                        e0.record(s)
-                        graph.replay()
-                        e1.record(s)
-                    e1.synchronize()
-                    out.append(e0.elapsed_time(e1) * 1e3 / calls)
-                return round(statistics.median(out), 3)
-
-            with torch.cuda.stream(s):
-                for i in range(min(nsets, 8)):
-                    call(i)
-            torch.cuda.synchronize()
-            gw = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gw, stream=s):
-                for _ in range(reps):
-                    call(0)
-            gc = torch.cuda.CUDAGraph()
-            ncold = max(reps, nsets)
-            with torch.cuda.graph(gc, stream=s):
-                for k in range(ncold):
-                    call(k % nsets)
-            with torch.cuda.stream(s):
-                gw.replay()
-                gc.replay()
-            torch.cuda.synchronize()
-            res[f"M{M}_N{N}"] = {"warm_us": timed(gw, reps), "cold_us": timed(gc, ncold),
-                                 "cold_sets": nsets,
-                                 "cluster": binding.attnres_plan(M, N, H)["cluster"]}
-            del gw, gc, P, A, A2, B, O, NP
-            torch.cuda.synchronize()
+            r = _decode_shape_times(binding, M, N, {"auto": None}, seed=900 + M * 16 + N)["auto"]
+            res[f"M{M}_N{N}"] = {"warm_us": r["warm_us"], "cold_us": r["cold_us"],
+                                 "cold_sets": r["cold_sets"], "variant": r["plan"]["variant"],
+                                 "cluster": r["plan"]["cluster"]}
     return res
+
+
+def single_cta_vs_cluster(binding):
+    """The one-CTA-per-token variant (variant 1, the pages' single-CTA kernel
+    for small N, TensorRT-LLM PR #20546 section "Op") against the automatic
+    choice (a cluster of CTAs per token) where the single CTA is meant to
+    serve: M in {1, 8}, N in {1..4}, warm and cold microseconds per call."""
+    res = {}
+    for M in (1, 8):
+        for N in (1, 2, 3, 4):
+            r = _decode_shape_times(binding, M, N, {"auto": None,
+                                                    "single_cta": binding.make_config("cta")},
+                                    seed=300 + M * 16 + N)
+            res[f"M{M}_N{N}"] = {k: {"warm_us": v["warm_us"], "cold_us": v["cold_us"],
+                                     "variant": v["plan"]["variant"], "cluster": v["plan"]["cluster"]}
+                                 for k, v in r.items()}
+    return res
+
+
+def pattern_ceiling(binding, inp, nbytes, peak, steps=10, warmup=3):
+    """GB/s of attnres_access_pattern on the bandwidth workload: the fused
+    op's loads, stores, grid and L2 prefetch without its arithmetic (CUDA
+    events around each launch on its stream, average)."""
+    import torch
+    s = torch.cuda.Stream()
+    out, newp = torch.empty_like(inp.prefix), torch.empty_like(inp.prefix)
+
+    def call():
+        binding.attnres_access_pattern(inp.prefix, inp.add, inp.add2, inp.bank, out, newp, stream=s)
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with torch.cuda.stream(s):
+        for a, b in ev:
+            a.record(s)
+            call()
+            b.record(s)
+    torch.cuda.synchronize()
+    avg = sum(a.elapsed_time(b) for a, b in ev) / steps / 1e3
+    nb = nbytes - 4 * H          # no w, gamma
+    del out, newp
+    return {"gbs": round(nb / avg / 1e9, 1), "avg_launch_us": round(avg * 1e6, 2),
+            "frac_of_peak": round(nb / avg / 1e9 / peak, 4),
+            "what": "attnres_access_pattern: same loads, stores, grid and L2 prefetch, no arithmetic"}
 
 
 def _graph_us(build_calls, s, replays=20):
@@ -732,8 +791,15 @@ def run_ours(args):
     deep = None
     fp16 = None
     cpu_base = None
+    single = None
+    ceiling = None
+    if default_workload and config is None:
+        ceiling = pattern_ceiling(binding, inp, nbytes, peaks()[0])
+        # the fused kernel's GB/s per launch as a fraction of the pattern's
+        ceiling["fused_over_pattern"] = round(nbytes / avg_launch / 1e9 / ceiling["gbs"], 4)
     if rank == 0 and not args.no_decode:
         decode = decode_latencies(binding, wl)
+        single = single_cta_vs_cluster(binding)
         comp = comparators(binding)
         chain = chain_benchmark(binding, wl)
         deep = deep_banks(binding, wl, peaks()[0])
@@ -792,7 +858,9 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
+        "pattern_ceiling": ceiling,
         "decode_us_per_call": decode,
+        "single_cta_vs_cluster_us": single,
         "fused_vs_alone_and_tail_add_us": comp,
         "chain_25_layers": chain,
         "deep_banks": deep,

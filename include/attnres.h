@@ -252,6 +252,23 @@ int attnres_tail_add(const void* prefix, const void* add, const void* add2,
 int attnres_tail_add_f16(const void* prefix, const void* add, const void* add2,
                          void* new_prefix, int M, int H, attnres_stream_t stream);
 
+/*
+ * attnres_access_pattern -- a measurement aid, not part of the op: the
+ * memory traffic of attnres_add_rmsnorm (both addends) without its
+ * arithmetic.  It runs with the launch configuration attnres_add_rmsnorm
+ * would choose for (M, N, H) -- the same clusters, grid, 16-byte loads of
+ * prefix, add, add2 and bank[0..N-1], the same L2 prefetch of the next token
+ * and the same two 16-byte stores per chunk -- but computes no fold, sums,
+ * exchanges or mixture: new_prefix receives a copy of prefix and out the XOR
+ * of the N+3 input rows (bit patterns).  The time of this call is the
+ * ceiling the fused op's access pattern can reach on this GPU.
+ * 0 <= N <= 12; add2 must be non-NULL; other rules as attnres_add_rmsnorm
+ * (w and gamma are not needed).
+ */
+int attnres_access_pattern(const void* prefix, const void* add, const void* add2,
+                           const void* bank, void* out, void* new_prefix,
+                           int M, int N, int H, attnres_stream_t stream);
+
 /* All arguments of one call, for attnres_launch. */
 typedef struct {
   const void* prefix;

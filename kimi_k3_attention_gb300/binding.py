@@ -32,6 +32,7 @@ EXPORTS = (
     "attnres_rmsnorm",
     "attnres_tail_add",
     "attnres_tail_add_f16",
+    "attnres_access_pattern",
     "attnres_launch",
     "attnres_plan",
     "attnres_status_string",
@@ -101,6 +102,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attnres_tail_add.restype = i
     lib.attnres_tail_add_f16.argtypes = [vp, vp, vp, vp, i, i, vp]
     lib.attnres_tail_add_f16.restype = i
+    lib.attnres_access_pattern.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, vp]
+    lib.attnres_access_pattern.restype = i
     lib.attnres_launch.argtypes = [ctypes.POINTER(Args), ctypes.POINTER(Config), vp]
     lib.attnres_launch.restype = i
     lib.attnres_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
@@ -254,6 +257,19 @@ def attnres_tail_add(prefix, add, add2, new_prefix, stream=None):
     lib = load()
     fn = lib.attnres_tail_add_f16 if code == DTYPE_FP16 else lib.attnres_tail_add
     _check(fn(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(new_prefix), M, H, _stream_handle(stream)))
+
+
+def attnres_access_pattern(prefix, add, add2, bank, out, new_prefix, stream=None):
+    """The fused op's memory traffic without its arithmetic (a measurement
+    aid): new_prefix = prefix, out = XOR of the N+3 input rows."""
+    N, M, H = bank.shape
+    dt = prefix.dtype
+    for name, t, shp in (("prefix", prefix, (M, H)), ("add", add, (M, H)), ("add2", add2, (M, H)),
+                         ("bank", bank, (N, M, H)), ("out", out, (M, H)),
+                         ("new_prefix", new_prefix, (M, H))):
+        _check_tensor(name, t, shp, dt)
+    _check(load().attnres_access_pattern(_ptr(prefix), _ptr(add), _ptr(add2), _ptr(bank), _ptr(out),
+                                         _ptr(new_prefix), M, N, H, _stream_handle(stream)))
 
 
 def launch(prefix, add, add2, bank, w, gamma, eps, out, new_prefix, h_out=None, M=None, N=None,

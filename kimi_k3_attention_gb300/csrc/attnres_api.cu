@@ -602,6 +602,61 @@ extern "C" int attnres_tail_add_f16(const void* prefix, const void* add, const v
   return tail_add(prefix, add, add2, new_prefix, M, H, ATTNRES_DTYPE_FP16, stream);
 }
 
+namespace attnres {
+namespace {
+
+cudaError_t dispatch_pattern(int N, const Params& p, dim3 g, int t, int c, cudaStream_t s) {
+#define ATTNRES_CASE(n) \
+  case n:               \
+    return launch_pattern<n>(p, g, t, c, s);
+  switch (N) {
+    ATTNRES_CASE(0)
+    ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
+    ATTNRES_CASE(5) ATTNRES_CASE(6) ATTNRES_CASE(7) ATTNRES_CASE(8)
+    ATTNRES_CASE(9) ATTNRES_CASE(10) ATTNRES_CASE(11) ATTNRES_CASE(12)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef ATTNRES_CASE
+}
+
+}  // namespace
+}  // namespace attnres
+
+extern "C" int attnres_access_pattern(const void* prefix, const void* add, const void* add2,
+                                      const void* bank, void* out, void* new_prefix, int M, int N,
+                                      int H, attnres_stream_t stream) {
+  if (!add2) return ATTNRES_ERR_NULL;
+  if (N > kShallowMaxN) return ATTNRES_ERR_SHAPE;
+  // the same checks as the fused call (w and gamma are not read: stand-ins)
+  Args a = make_args(prefix, add, add2, bank, prefix, prefix, 1.0f, out, new_prefix, nullptr, M,
+                     N, H, true);
+  int st = validate(a);
+  if (st != ATTNRES_OK) return st;
+  int sms = 0;
+  if ((st = current_device(&sms)) != ATTNRES_OK) return st;
+  attnres_config c = {0, 0, 0, 0, 0, 0, 0};
+  if ((st = resolve(M, N, true, H, sms, &c)) != ATTNRES_OK) return st;
+  if (c.threads > kPatternMaxT) return ATTNRES_ERR_CONFIG;
+  Params p = {};
+  p.prefix = static_cast<const uint4*>(prefix);
+  p.add = static_cast<const uint4*>(add);
+  p.add2 = static_cast<const uint4*>(add2);
+  p.bank = static_cast<const uint4*>(bank);
+  p.out = static_cast<uint4*>(out);
+  p.new_prefix = static_cast<uint4*>(new_prefix);
+  p.M = M;
+  p.H8 = H / 8;
+  p.bank_stride = static_cast<long long>(M) * p.H8;
+  p.cpc = (p.H8 + c.cluster - 1) / c.cluster;
+  p.prefetch = c.prefetch > 0 ? c.prefetch : 0;
+  const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
+  cudaError_t e = dispatch_pattern(N, p, grid, c.threads, c.cluster,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ATTNRES_OK;
+}
+
 extern "C" int attnres_plan(int M, int N, int H, int has_add2, attnres_config* plan) {
   if (!plan) return ATTNRES_ERR_NULL;
   if (validate_shape(M, N, H) != ATTNRES_OK) return ATTNRES_ERR_SHAPE;

@@ -84,6 +84,9 @@ constexpr unsigned int kStatusWaitTimeout = 1u;
 
 constexpr unsigned FULL = 0xffffffffu;
 
+// Threads per CTA of the access-pattern kernel (at most).
+constexpr int kPatternMaxT = 256;
+
 // ---------------------------------------------------------------- PTX helpers
 
 // Global loads.  Each is volatile with a memory clobber, so the compiler
@@ -153,6 +156,19 @@ __device__ __forceinline__ void unpack_f32x2(unsigned long long v, float& lo, fl
 __device__ __forceinline__ void fma_rn_x2(unsigned long long& acc, unsigned long long a,
                                           unsigned long long b) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+// Both halves: a * b, each rounded to nearest even, subnormals kept.
+__device__ __forceinline__ unsigned long long mul_rn_x2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+__device__ __forceinline__ float add_rn(float a, float b) {
+  float r;
+  asm("add.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 
 __device__ __forceinline__ float mul_rn(float a, float b) {
@@ -739,18 +755,19 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
   float q = 0.f;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
-    {
-      const uint4 u = src.get(0, k);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) h[k][e] = mul_rn(alpha[0], elem<DT>(u, e));
-    }
     if constexpr (VPT == 1) {
-      // the remaining sources with packed float32x2 FMAs (each lane an
-      // fma.rn.f32: the same bits as the scalar form, half the FMA
-      // instructions; GB300, M = 8192, N = 12: +2 % bandwidth)
+      // packed float32x2 arithmetic (each lane a mul.rn / fma.rn.f32: the
+      // same bits as the scalar form, half the instructions; GB300,
+      // M = 8192, N = 12: +2 % bandwidth for the FMAs)
       unsigned long long h2[4];
+      {
+        const uint4 u = src.get(0, k);
+        const unsigned long long a2 = pack_f32x2(alpha[0], alpha[0]);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int q2 = 0; q2 < 4; ++q2) h2[q2] = pack_f32x2(h[k][2 * q2], h[k][2 * q2 + 1]);
+        for (int q2 = 0; q2 < 4; ++q2)
+          h2[q2] = mul_rn_x2(a2, pack_f32x2(Fmt<DT>::lo(w4[q2]), Fmt<DT>::hi(w4[q2])));
+      }
 #pragma unroll
       for (int i = 1; i < S; ++i) {
         const uint4 u = src.get(i, k);
@@ -760,20 +777,32 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
         for (int q2 = 0; q2 < 4; ++q2)
           fma_rn_x2(h2[q2], a2, pack_f32x2(Fmt<DT>::lo(w4[q2]), Fmt<DT>::hi(w4[q2])));
       }
+      // sum of squares: even and odd columns in the two lanes, then added
+      unsigned long long q2 = pack_f32x2(0.f, 0.f);
 #pragma unroll
-      for (int q2 = 0; q2 < 4; ++q2) unpack_f32x2(h2[q2], h[k][2 * q2], h[k][2 * q2 + 1]);
+      for (int j = 0; j < 4; ++j) fma_rn_x2(q2, h2[j], h2[j]);
+      float qe, qo;
+      unpack_f32x2(q2, qe, qo);
+      q = add_rn(qe, qo);
+#pragma unroll
+      for (int q2i = 0; q2i < 4; ++q2i) unpack_f32x2(h2[q2i], h[k][2 * q2i], h[k][2 * q2i + 1]);
     } else {
       // two chunks per thread: the packed form costs more registers than it
       // saves instructions
+      {
+        const uint4 u = src.get(0, k);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[k][e] = mul_rn(alpha[0], elem<DT>(u, e));
+      }
 #pragma unroll
       for (int i = 1; i < S; ++i) {
         const uint4 u = src.get(i, k);
 #pragma unroll
         for (int e = 0; e < 8; ++e) h[k][e] = fma_rn(alpha[i], elem<DT>(u, e), h[k][e]);
       }
-    }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) q = fma_rn(h[k][e], h[k][e], q);
+      for (int e = 0; e < 8; ++e) q = fma_rn(h[k][e], h[k][e], q);
+    }
   }
 
   // ---- R2: warp sum, lane c stores it into CTA c, every warp sums all
@@ -807,15 +836,20 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
         hv.w = Fmt<DT>::pack(h[k][6], h[k][7]);
         st_out(p.h_out + row + jj[k], t.failed ? nan4 : hv);
       }
-      uint4 o;
-      o.x = Fmt<DT>::pack(mul_rn(mul_rn(h[k][0], rh), elem<DT>(gv[k], 0)),
-                          mul_rn(mul_rn(h[k][1], rh), elem<DT>(gv[k], 1)));
-      o.y = Fmt<DT>::pack(mul_rn(mul_rn(h[k][2], rh), elem<DT>(gv[k], 2)),
-                          mul_rn(mul_rn(h[k][3], rh), elem<DT>(gv[k], 3)));
-      o.z = Fmt<DT>::pack(mul_rn(mul_rn(h[k][4], rh), elem<DT>(gv[k], 4)),
-                          mul_rn(mul_rn(h[k][5], rh), elem<DT>(gv[k], 5)));
-      o.w = Fmt<DT>::pack(mul_rn(mul_rn(h[k][6], rh), elem<DT>(gv[k], 6)),
-                          mul_rn(mul_rn(h[k][7], rh), elem<DT>(gv[k], 7)));
+      // (h * r_h) * gamma, two lanes per instruction, each product rounded
+      const unsigned long long rh2 = pack_f32x2(rh, rh);
+      const uint32_t g4[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
+      uint32_t o4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const unsigned long long v2 =
+            mul_rn_x2(mul_rn_x2(pack_f32x2(h[k][2 * j], h[k][2 * j + 1]), rh2),
+                      pack_f32x2(Fmt<DT>::lo(g4[j]), Fmt<DT>::hi(g4[j])));
+        float lo, hi;
+        unpack_f32x2(v2, lo, hi);
+        o4[j] = Fmt<DT>::pack(lo, hi);
+      }
+      const uint4 o = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       st_out(p.out + row + jj[k], t.failed ? nan4 : o);
     }
   }
@@ -938,8 +972,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
       }
     }
     // Let the next kernel on the stream be scheduled once every CTA of this
-    // grid is past its loads; it still waits for this grid to finish.
-    griddep_launch_dependents();
+    // grid is past its first loads; it still waits for this grid to finish.
+    if (m == static_cast<int>(blockIdx.y)) griddep_launch_dependents();
     if (!early_init && m == static_cast<int>(blockIdx.y)) exchange_init<Sums<N>::total>(x, t, p);
     if constexpr (HYB) {
       cp_async_wait<0>();   // this thread's own slots: no barrier needed
@@ -1054,6 +1088,55 @@ __global__ void __launch_bounds__(256) attnres_tail_add_kernel(const uint4* pref
   griddep_launch_dependents();
 }
 
+// The access pattern of the streaming fused kernel without its arithmetic:
+// the same grid of clusters walking tokens, the same 16-byte loads of every
+// row chunk (prefix, add, add2, bank[0..N-1]), the same next-token L2
+// prefetch and the same two 16-byte stores per chunk, but no fold, sums,
+// exchanges or mixture: new_prefix receives the prefix chunk and out the XOR
+// of all loaded chunks (which keeps every load live).  A measurement of how
+// fast this GPU serves the fused kernel's traffic, not a result.
+template <int N>
+__global__ void __launch_bounds__(kPatternMaxT) attnres_pattern_kernel(const Params p) {
+  const int c0 = static_cast<int>(cluster_ctarank()) * p.cpc;
+  const int cend = min(c0 + p.cpc, p.H8);
+  const int j = c0 + static_cast<int>(threadIdx.x);
+  const bool ok = j < cend;
+  griddep_wait();
+  for (int m = blockIdx.y; m < p.M; m += gridDim.y) {
+    const size_t row = static_cast<size_t>(m) * p.H8;
+    uint4 v[N + 3];
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    v[0] = ok ? ld_prefix(p.prefix + row + j) : z;
+    v[1] = ok ? ld_stream(p.add + row + j) : z;
+    v[2] = ok ? ld_stream(p.add2 + row + j) : z;
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[3 + i] = ok ? ld_stream(p.bank + i * p.bank_stride + row + j) : z;
+    if ((p.prefetch & 4) && m + static_cast<int>(gridDim.y) < p.M) {
+      constexpr int rows = N + 3;
+      if (static_cast<int>(threadIdx.x) < rows && cend > c0) {
+        const int r = threadIdx.x;
+        const size_t off = static_cast<size_t>(m + gridDim.y) * p.H8 + c0;
+        const uint4* src = r < N ? p.bank + r * p.bank_stride + off
+                         : r == N ? p.prefix + off : r == N + 1 ? p.add + off : p.add2 + off;
+        prefetch_l2(src, static_cast<uint32_t>(cend - c0) * 16u);
+      }
+    }
+    griddep_launch_dependents();
+    uint4 x = v[0];
+#pragma unroll
+    for (int i = 1; i < N + 3; ++i) {
+      x.x ^= v[i].x;
+      x.y ^= v[i].y;
+      x.z ^= v[i].z;
+      x.w ^= v[i].w;
+    }
+    if (ok) {
+      st_out(p.new_prefix + row + j, v[0]);
+      st_out(p.out + row + j, x);
+    }
+  }
+}
+
 // Host-side launchers of one instantiation (defined in attnres_launch.cuh).
 template <int N, int MODE, int VPT, int MAXT, int MINB, int DT = kBF16, int NR = N>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
@@ -1065,5 +1148,7 @@ template <bool ADD2, int DT>
 cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* add2,
                             uint4* new_prefix, long long chunks, int sms, bool pdl,
                             cudaStream_t s);
+template <int N>
+cudaError_t launch_pattern(const Params& p, dim3 grid, int threads, int cluster, cudaStream_t s);
 
 }  // namespace attnres

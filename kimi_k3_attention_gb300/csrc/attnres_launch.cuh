@@ -173,6 +173,39 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
                             chunks);
 }
 
+// The access-pattern kernel: one thread per chunk of the CTA's columns, a
+// cluster of `cluster` CTAs per token, grid.y clusters walking the tokens.
+template <int N>
+cudaError_t launch_pattern(const Params& p, dim3 grid, int threads, int cluster, cudaStream_t s) {
+  auto kern = attnres_pattern_kernel<N>;
+  static std::atomic<unsigned char> opted[kMaxDevices];
+  if (cluster > 8) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!opted[dev].load(std::memory_order_acquire)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      opted[dev].store(1, std::memory_order_release);
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 // Instantiations.  Each attnres_inst_*.cu unit expands its share with DEF
 // empty (explicit instantiation definitions, where the kernels are
 // compiled); the API unit expands all of them with DEF = extern, so that it
@@ -238,6 +271,14 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   ATTNRES_TAIL_ADD(DEF, true, kBF16) ATTNRES_TAIL_ADD(DEF, false, kBF16)     \
   ATTNRES_TAIL_ADD(DEF, true, kFP16) ATTNRES_TAIL_ADD(DEF, false, kFP16)
 
+#define ATTNRES_PATTERN(DEF, N) \
+  DEF template cudaError_t launch_pattern<N>(const Params&, dim3, int, int, cudaStream_t);
+#define ATTNRES_INSTANTIATE_PATTERN(DEF)                                                       \
+  ATTNRES_PATTERN(DEF, 0) ATTNRES_PATTERN(DEF, 1) ATTNRES_PATTERN(DEF, 2) ATTNRES_PATTERN(DEF, 3) \
+  ATTNRES_PATTERN(DEF, 4) ATTNRES_PATTERN(DEF, 5) ATTNRES_PATTERN(DEF, 6) ATTNRES_PATTERN(DEF, 7) \
+  ATTNRES_PATTERN(DEF, 8) ATTNRES_PATTERN(DEF, 9) ATTNRES_PATTERN(DEF, 10)                      \
+  ATTNRES_PATTERN(DEF, 11) ATTNRES_PATTERN(DEF, 12)
+
 // Which unit defines what.
 #define ATTNRES_UNIT_A(DEF)                                                             \
   ATTNRES_INSTANTIATE(DEF, 1, true) ATTNRES_INSTANTIATE(DEF, 2, true)                   \
@@ -263,7 +304,8 @@ cudaError_t launch_tail_add(const uint4* prefix, const uint4* add, const uint4* 
   ATTNRES_INSTANTIATE_NOFOLD(DEF, 6) ATTNRES_INSTANTIATE_NOFOLD(DEF, 7)                 \
   ATTNRES_INSTANTIATE_NOFOLD(DEF, 8) ATTNRES_INSTANTIATE_NOFOLD(DEF, 9)                 \
   ATTNRES_INSTANTIATE_NOFOLD(DEF, 10) ATTNRES_INSTANTIATE_NOFOLD(DEF, 11)               \
-  ATTNRES_INSTANTIATE_NOFOLD(DEF, 12) ATTNRES_INSTANTIATE_TAIL_ADD(DEF)
+  ATTNRES_INSTANTIATE_NOFOLD(DEF, 12) ATTNRES_INSTANTIATE_TAIL_ADD(DEF)               \
+  ATTNRES_INSTANTIATE_PATTERN(DEF)
 #define ATTNRES_UNIT_F(DEF)                                                             \
   ATTNRES_INSTANTIATE_DEEP(DEF, 13) ATTNRES_INSTANTIATE_DEEP(DEF, 14)                   \
   ATTNRES_INSTANTIATE_DEEP(DEF, 15) ATTNRES_INSTANTIATE_DEEP(DEF, 16)                   \

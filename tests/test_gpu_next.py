@@ -145,3 +145,22 @@ def test_no_snapshots(add2):
     ref = torch.nn.functional.rms_norm(inp.prefix.double(), (H,), inp.gamma.double(),
                                        float(np.float32(inp.eps))).numpy()
     assert check_out(u16(out), ref, np.abs(ref) + 1e-30)["ok"]
+
+
+@pytest.mark.parametrize("M,N,Hs", [(8192, 12, 7168), (5, 3, 7168), (300, 0, 2056), (33, 12, 64)])
+def test_access_pattern_measurement_aid(M, N, Hs):
+    """attnres_access_pattern (the fused op's traffic without its arithmetic):
+    new_prefix is a copy of prefix and out the XOR of the N+3 input rows."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(M + N)
+    rnd = lambda *sh: torch.randn(sh, generator=g, device="cuda").to(torch.bfloat16)  # noqa: E731
+    P, A, A2, B = rnd(M, Hs), rnd(M, Hs), rnd(M, Hs), rnd(N, M, Hs)
+    out, newp = Guarded((M, Hs)), Guarded((M, Hs))
+    binding.attnres_access_pattern(P, A, A2, B, out.t, newp.t)
+    torch.cuda.synchronize()
+    assert out.guards_intact() and newp.guards_intact()
+    assert (u16(newp.t) == u16(P)).all()
+    x = u16(P) ^ u16(A) ^ u16(A2)
+    for i in range(N):
+        x = x ^ u16(B[i])
+    assert (u16(out.t) == x).all()
