@@ -932,7 +932,7 @@ def main(argv=None):
                     help="bank snapshots N of the bandwidth workload (other values only for profiling)")
     ap.add_argument("--fp16", action="store_true",
                     help="FP16 tensors instead of BF16 (profiling)")
-    ap.add_argument("--variant", default="auto", choices=("auto", "cta", "cluster", "stream", "pipe"),
+    ap.add_argument("--variant", default="auto", choices=("auto", "cta", "cluster", "cluster2", "stream", "pipe"),
                     help="pin the launch variant of the bandwidth workload (profiling)")
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)

@@ -136,7 +136,8 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *             5 = as 2 with registers capped so that two CTAs of up to 256
  *                 threads share an SM (in back-to-back calls the next
  *                 call's CTAs can become resident, and prefetch, while this
- *                 call runs);
+ *                 call runs); the automatic choice from 17 to 32 tokens
+ *                 when the call folds BF16 tensors and N <= 12;
  *             Variants 1, 4 and 5 exist for N <= 12 only (variant 5 with
  *             the fold on BF16 tensors only).  For N > 12
  *             variant 3 takes at most 128 threads, registers capped so
@@ -169,9 +170,13 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *             its first token; 2 = let the next kernel be scheduled at once;
  *             4 = while a token is reduced, ask L2 for the CTA's rows of the
  *             next token it takes (when clusters walk several tokens);
- *             -1 = none; 0 = the default (1 up to 96 tokens, plus 4 when the
- *             grid is smaller than M).  A prefetch is a hint to a coherent L2
- *             and cannot change results.
+ *             8 = before waiting on the previous kernel, read one 32-bit
+ *             word of every 128-byte line of this CTA's rows of its first
+ *             token through L2 (values discarded, nothing allocated in L1):
+ *             lines an SM has read reach it sooner than lines only
+ *             prefetched; -1 = none; 0 = the default (1 + 8 up to 96
+ *             tokens, plus 4 when the grid is smaller than M).  These reads
+ *             are hints to a coherent L2 and cannot change results.
  */
 typedef struct {
   int variant;

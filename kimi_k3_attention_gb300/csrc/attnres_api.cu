@@ -159,9 +159,10 @@ int round_up32(int x) { return (x + 31) & ~31; }
 constexpr size_t kPipeSmemMax = 227 * 1024 - sizeof(Exchange<1>) - 1024;
 
 // Fill every zero field of *c for (M, N, H) on a device with `sms` SMs, then
-// check the result.  Returns ATTNRES_OK or ATTNRES_ERR_CONFIG.
-
-int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
+// check the result.  bf16_fold: the call folds BF16 tensors (the shapes
+// compiled for that case only may be chosen).  Returns ATTNRES_OK or
+// ATTNRES_ERR_CONFIG.
+int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c, bool bf16_fold) {
   const int H8 = H / 8;
   auto min_cluster = [&](int maxt) {
     int cl = 1;
@@ -176,17 +177,20 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
   if (c->variant == 0) {
     // Measured on GB300 at H = 7168 (the cluster sizes below are for that
     // H and scale with it): up to 32 tokens, a cluster of about 128 / M CTAs
-    // (clamped to 4..8) per token keeps ~128 CTAs per call, one per SM; up
-    // to 48 tokens, 8 CTAs of 112 columns (three fit an SM, still one
-    // wave); then the register-capped shape, 4 CTAs of 224 columns up to 96
-    // tokens and 7 CTAs of 128 columns beyond, where many tokens are in
-    // flight on every SM.  Deep banks: up to 32 tokens the same clusters
-    // (4 CTAs from 8 tokens on once N >= 24, where a token's rows are many),
-    // beyond that their streaming shape, 7 CTAs of 128 columns (the split
-    // shape's CTAs hold too many registers to share an SM).
+    // (clamped to 4..8) per token keeps ~128 CTAs per call, one per SM; from
+    // 17 tokens on (4 CTAs of 224 threads) with registers capped so that
+    // the next call's CTAs fit beside them (0.05-0.16 us faster there, the
+    // same below); up to 48 tokens, 8 CTAs of 112 columns (three fit an SM,
+    // still one wave); then the register-capped shape, 4 CTAs of 224
+    // columns up to 96 tokens and 7 CTAs of 128 columns beyond, where many
+    // tokens are in flight on every SM.  Deep banks: up to 32 tokens the
+    // same clusters (4 CTAs from 8 tokens on once N >= 24, where a token's
+    // rows are many), beyond that their streaming shape, 7 CTAs of 128
+    // columns (the split shape's CTAs hold too many registers to share an
+    // SM).
     int ref;
     if (M <= 32) {
-      c->variant = 2;
+      c->variant = (M >= 17 && bf16_fold && !deep) ? 5 : 2;
       ref = (128 + M / 2) / M;
       ref = ref < 4 ? 4 : (ref > 8 ? 8 : ref);
       if (N >= 24 && M >= 8) ref = 4;
@@ -204,7 +208,7 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
       ref = 7;
     }
     if (c->cluster == 0) {
-      const int lo = min_cluster(c->variant == 2 ? kSplitMaxT : stream_maxt);
+      const int lo = min_cluster(c->variant == 3 ? stream_maxt : kSplitMaxT);
       int cl = (ref * H8 + 448) / 896;
       c->cluster = cl < lo ? lo : (cl > 16 ? 16 : cl);
     }
@@ -274,10 +278,10 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c) {
   }
   if (c->pdl < -1 || c->pdl > 1) return ATTNRES_ERR_CONFIG;
   if (c->pdl == 0) c->pdl = 1;
-  if (c->prefetch < -1 || c->prefetch > 7) return ATTNRES_ERR_CONFIG;
+  if (c->prefetch < -1 || c->prefetch > 15) return ATTNRES_ERR_CONFIG;
   if (c->prefetch == 0) {
     const bool fused = c->variant == 2 || c->variant == 3 || c->variant == 5;
-    c->prefetch = (fused && M <= 96) ? 1 : 0;
+    c->prefetch = (fused && M <= 96) ? 1 | 8 : 0;
     if (fused && c->grid_tokens < M) c->prefetch |= 4;   // clusters walk tokens
     if (c->prefetch == 0) c->prefetch = -1;
   }
@@ -409,7 +413,9 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   if ((st = current_device(&sms)) != ATTNRES_OK) return st;
   const bool has_add2 = a.fold && a.add2 != nullptr;
   attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0, 0, 0};
-  if ((st = resolve(a.M, a.N, has_add2, a.H, sms, &c)) != ATTNRES_OK) return st;
+  if ((st = resolve(a.M, a.N, has_add2, a.H, sms, &c, a.fold && a.dtype == ATTNRES_DTYPE_BF16)) !=
+      ATTNRES_OK)
+    return st;
   // the attention-residual alone and FP16 tensors exist in the two fused
   // shapes only
   if ((!a.fold || a.dtype == ATTNRES_DTYPE_FP16) && c.variant != 2 && c.variant != 3)
@@ -636,7 +642,7 @@ extern "C" int attnres_access_pattern(const void* prefix, const void* add, const
   int sms = 0;
   if ((st = current_device(&sms)) != ATTNRES_OK) return st;
   attnres_config c = {0, 0, 0, 0, 0, 0, 0};
-  if ((st = resolve(M, N, true, H, sms, &c)) != ATTNRES_OK) return st;
+  if ((st = resolve(M, N, true, H, sms, &c, true)) != ATTNRES_OK) return st;
   if (c.threads > kPatternMaxT) return ATTNRES_ERR_CONFIG;
   Params p = {};
   p.prefix = static_cast<const uint4*>(prefix);
@@ -664,7 +670,7 @@ extern "C" int attnres_plan(int M, int N, int H, int has_add2, attnres_config* p
   int st = current_device(&sms);
   if (st != ATTNRES_OK) return st;
   attnres_config c = {0, 0, 0, 0, 0, 0, 0};
-  if ((st = resolve(M, N, has_add2 != 0, H, sms, &c)) != ATTNRES_OK) return st;
+  if ((st = resolve(M, N, has_add2 != 0, H, sms, &c, true)) != ATTNRES_OK) return st;
   *plan = c;
   return ATTNRES_OK;
 }

@@ -69,7 +69,10 @@ struct Params {
   int prefetch;           // bit 0: warm L2 with the first token's rows before
                           // waiting on the previous kernel; bit 1: also let the
                           // next kernel be scheduled at once; bit 2: while a
-                          // token is reduced, warm L2 with the next token's rows
+                          // token is reduced, warm L2 with the next token's rows;
+                          // bit 3: before waiting, read one word of every
+                          // 128-byte line of the first token's rows (see
+                          // attnres_fused_kernel)
 };
 
 // What a launch does with the prefix sum.
@@ -92,26 +95,24 @@ constexpr int kPatternMaxT = 256;
 // Global loads.  Each is volatile with a memory clobber, so the compiler
 // keeps it after griddep_wait(): under programmatic dependent launch the
 // data may be written by the previous kernel on the stream.
-//   ld_stream: read once, not kept in L1, through the non-coherent path;
-//              only for tensors no thread of the kernel writes
-//   ld_prefix: read once, not kept in L1, coherent; for the prefix sum,
-//              which the call may overwrite in place with the new prefix
+//   ld_stream: a row chunk, read once, not kept in L1, coherent (plain
+//              ld.global: the prefix may be overwritten in place by the
+//              same call, and on GB300 this form decodes slightly faster
+//              than the non-coherent one)
 //   ld_keep:   small read-only vectors (w, gamma), cached
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p)
                : "memory");
   return r;
 }
 
-__device__ __forceinline__ uint4 ld_prefix(const uint4* p) {
-  uint4 r;
-  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p)
-               : "memory");
+// One 32-bit word through L2 only (never allocated in L1).
+__device__ __forceinline__ uint32_t ld_l2_word(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
   return r;
 }
 
@@ -435,6 +436,18 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// The sum of L values (a power of two) in the order of an XOR butterfly over
+// L lanes (offsets L/2, ..., 1): the bits every lane of warp_sum (L = 32) or
+// half_warp_sum (L = 16) ends with when lane i starts with e[i].
+template <int L>
+__device__ __forceinline__ float butterfly_order_sum(float (&e)[L]) {
+#pragma unroll
+  for (int h = L / 2; h >= 1; h >>= 1)
+#pragma unroll
+    for (int i = 0; i < h; ++i) e[i] = e[i] + e[i + h];
+  return e[0];
+}
+
 // Transpose-reduction of KP (a power of two <= 32) values per lane across the
 // warp with KP-1 + (5 - log2 KP) shuffles.  Afterwards lane l holds the warp
 // total of value index l >> (5 - log2 KP); lanes sharing an index agree.
@@ -506,7 +519,7 @@ struct Sums {
 // and the transaction count never runs ahead of its arming.  No CTA reads
 // another's shared memory, so there is no barrier at exit.
 template <int G>
-struct Exchange {
+struct alignas(16) Exchange {
   float red[16][32 * G];   // up to 16 warps (448-thread CTAs have 14)
   float xin1[16][32 * G];  // up to 16 CTAs per cluster
   float xin2[256];         // 16 CTAs x 16 warps
@@ -652,8 +665,9 @@ __device__ __forceinline__ void source_sums(const Src& src, const uint4 (&wv)[VP
 // softmax, mixture, and the two stores.  pr/ad/ad2 are the token's prefix and
 // addend chunks, src gives the bank chunks (and receives the updated prefix),
 // wv the pseudo-query chunks; masked chunks (ok false) are zeros and store
-// nothing.
-template <int N, int MODE, int VPT, int DT, class Src>
+// nothing.  LAT (the latency shapes) adds the R2 partials in every lane
+// instead of with shuffles: the same bits, a shorter dependent chain.
+template <int N, int MODE, int VPT, int DT, bool LAT, class Src>
 __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>::G>& x, Thread& t,
                                                size_t row, const int (&jj)[VPT],
                                                const bool (&ok)[VPT], const uint4 (&wv)[VPT],
@@ -816,8 +830,27 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
   t.phase ^= 1u;
   const int nw_total = static_cast<int>(t.csize) * t.nwarps;
   float qq = 0.f;
-  for (int idx = lane; idx < nw_total; idx += 32) qq += x.xin2[idx];
-  qq = warp_sum(qq);
+  if constexpr (LAT) {
+    // every lane adds all partials itself: v[l] as lane l would (xin2[l],
+    // xin2[l + 32], ... in order), then the butterfly's pairing of lanes
+    float v[32];
+#pragma unroll
+    for (int l = 0; l < 32; ++l) v[l] = 0.f;
+    for (int base = 0; base < nw_total; base += 32) {
+#pragma unroll
+      for (int l4 = 0; l4 < 8; ++l4) {
+        const float4 f = *reinterpret_cast<const float4*>(&x.xin2[base + 4 * l4]);
+        if (base + 4 * l4 < nw_total) v[4 * l4] += f.x;
+        if (base + 4 * l4 + 1 < nw_total) v[4 * l4 + 1] += f.y;
+        if (base + 4 * l4 + 2 < nw_total) v[4 * l4 + 2] += f.z;
+        if (base + 4 * l4 + 3 < nw_total) v[4 * l4 + 3] += f.w;
+      }
+    }
+    qq = butterfly_order_sum<32>(v);
+  } else {
+    for (int idx = lane; idx < nw_total; idx += 32) qq += x.xin2[idx];
+    qq = warp_sum(qq);
+  }
   const float rh = rsqrtf(__fmaf_rn(qq, p.inv_h, p.eps));
 
   // ---- outputs (after a timed-out exchange wait the sums are partial: out
@@ -878,6 +911,9 @@ template <int N, int MODE, int VPT, int MAXT, int MINB, int DT = kBF16, int NR =
 __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params p) {
   constexpr bool HYB = NR < N;
   static_assert(!HYB || VPT == 1, "shared-memory rows take one chunk per thread");
+  // the latency shapes (split, split with two CTAs per SM, one CTA per
+  // token): at most a few warps per SM, latency rather than issue bound
+  constexpr bool LAT = (MINB <= 2) && (MAXT >= 256);
   __shared__ Exchange<Sums<N>::G> x;
   extern __shared__ __align__(16) uint4 hyb[];   // [N - NR][blockDim.x] when HYB
   Thread t = thread_info();
@@ -917,6 +953,27 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // here, overlapping the previous kernel's tail (shared memory only); in the
   // streaming regime after the first token's loads are issued, so that the
   // set-up does not delay them.
+  // Latency regime, bit 3: read one 32-bit word of every 128-byte line of
+  // this CTA's first-token rows, through L2 only, before the wait.  On
+  // GB300 (two dies) lines that an SM has read are served to it faster than
+  // lines only prefetched into L2 (cold decode calls: 0.2-0.4 us faster);
+  // the values are discarded (consumed only by an empty asm after the
+  // wait), and no L1 line is allocated, so the loads after the wait see the
+  // previous kernel's writes.
+  constexpr int WROWS = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3);
+  constexpr bool WARM = (VPT == 1) && !HYB;
+  uint32_t warm[WARM ? WROWS : 1];
+#pragma unroll
+  for (int r = 0; r < (WARM ? WROWS : 1); ++r) warm[r] = 0;
+  if constexpr (WARM) {
+    if ((p.prefetch & 8) && blockIdx.y < p.M && ok[0] && (jj[0] & 7) == 0) {
+      const size_t off = static_cast<size_t>(blockIdx.y) * p.H8 + jj[0];
+#pragma unroll
+      for (int r = 0; r < WROWS; ++r)
+        warm[r] = ld_l2_word(r < N ? p.bank + r * p.bank_stride + off
+                             : r == N ? p.prefix + off : r == N + 1 ? p.add + off : p.add2 + off);
+    }
+  }
   const bool early_init = p.prefetch != 0;
   if (early_init && blockIdx.y < p.M) exchange_init<Sums<N>::total>(x, t, p);
   // Programmatic dependent launch: this grid may have been scheduled while
@@ -924,6 +981,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // complete (and its writes to be visible) before reading its outputs.
   // Without the launch attribute this returns at once.
   griddep_wait();
+#pragma unroll
+  for (int r = 0; r < (WARM ? WROWS : 1); ++r) asm volatile("" ::"r"(warm[r]));
 
   uint4 wv[VPT], gv[VPT];
 #pragma unroll
@@ -940,7 +999,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const uint4 z = make_uint4(0, 0, 0, 0);
-      pr[k] = ok[k] ? ld_prefix(p.prefix + row + jj[k]) : z;
+      pr[k] = ok[k] ? ld_stream(p.prefix + row + jj[k]) : z;
       ad[k] = (MODE != kNoFold && ok[k]) ? ld_stream(p.add + row + jj[k]) : z;
       ad2[k] = (MODE == kFoldAdd2 && ok[k]) ? ld_stream(p.add2 + row + jj[k]) : z;
 #pragma unroll
@@ -978,10 +1037,10 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     if constexpr (HYB) {
       cp_async_wait<0>();   // this thread's own slots: no barrier needed
       HybridSources<N, NR> src{v, hyb0, hstep, ok[0]};
-      token_epilogue<N, MODE, VPT, DT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
+      token_epilogue<N, MODE, VPT, DT, LAT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
     } else {
       RegSources<N, VPT> src{v};
-      token_epilogue<N, MODE, VPT, DT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
+      token_epilogue<N, MODE, VPT, DT, LAT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
     }
   }
   exchange_exit(t, p);
@@ -1058,7 +1117,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
       a += row_step;
     }
     SmemSources<N> src{a, row_step, ok[0], z};
-    token_epilogue<N, ADD2 ? kFoldAdd2 : kFoldAdd, 1, kBF16>(p, x, t, static_cast<size_t>(m) * p.H8, jj,
+    token_epilogue<N, ADD2 ? kFoldAdd2 : kFoldAdd, 1, kBF16, false>(p, x, t, static_cast<size_t>(m) * p.H8, jj,
                                                      ok, wv, gv, pr, ad, ad2, src, first);
     stage = (stage + 1 == STAGES) ? 0 : stage + 1;
   }
@@ -1083,7 +1142,7 @@ __global__ void __launch_bounds__(256) attnres_tail_add_kernel(const uint4* pref
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += stride) {
     const uint4 a2 = ADD2 ? ld_stream(add2 + i) : make_uint4(0, 0, 0, 0);
-    st_out(new_prefix + i, fold_chunk<ADD2, DT>(ld_prefix(prefix + i), ld_stream(add + i), a2));
+    st_out(new_prefix + i, fold_chunk<ADD2, DT>(ld_stream(prefix + i), ld_stream(add + i), a2));
   }
   griddep_launch_dependents();
 }
@@ -1106,7 +1165,7 @@ __global__ void __launch_bounds__(kPatternMaxT) attnres_pattern_kernel(const Par
     const size_t row = static_cast<size_t>(m) * p.H8;
     uint4 v[N + 3];
     const uint4 z = make_uint4(0, 0, 0, 0);
-    v[0] = ok ? ld_prefix(p.prefix + row + j) : z;
+    v[0] = ok ? ld_stream(p.prefix + row + j) : z;
     v[1] = ok ? ld_stream(p.add + row + j) : z;
     v[2] = ok ? ld_stream(p.add2 + row + j) : z;
 #pragma unroll

@@ -279,7 +279,7 @@ def test_side_stream_and_plan():
     assert_parity(inp, gnp, gout)
     for M in (1, 8, 16, 32, 8192):
         plan = binding.attnres_plan(M, 12, H)
-        assert plan["variant"] in (1, 2, 3, 4) and plan["threads"] % 32 == 0
+        assert plan["variant"] in (1, 2, 3, 4, 5) and plan["threads"] % 32 == 0
 
 
 def test_invalid_config_rejected_on_device():
@@ -385,7 +385,7 @@ def test_pipe_invalid_stages_rejected():
         assert e.value.status == -8
 
 
-@pytest.mark.parametrize("prefetch", [-1, 1, 2, 3])
+@pytest.mark.parametrize("prefetch", [-1, 1, 2, 3, 8, 9, 15])
 def test_prefetch_modes_identical(prefetch):
     """L2 prefetch and early dependent launch change scheduling only; a
     dependent chain queued without host synchronisation stays exact."""
