@@ -278,10 +278,10 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c, bool bf1
   }
   if (c->pdl < -1 || c->pdl > 1) return ATTNRES_ERR_CONFIG;
   if (c->pdl == 0) c->pdl = 1;
-  if (c->prefetch < -1 || c->prefetch > 15) return ATTNRES_ERR_CONFIG;
+  if (c->prefetch < -1 || c->prefetch > 7) return ATTNRES_ERR_CONFIG;
   if (c->prefetch == 0) {
     const bool fused = c->variant == 2 || c->variant == 3 || c->variant == 5;
-    c->prefetch = (fused && M <= 96) ? 1 | 8 : 0;
+    c->prefetch = (fused && M <= 96) ? 1 : 0;
     if (fused && c->grid_tokens < M) c->prefetch |= 4;   // clusters walk tokens
     if (c->prefetch == 0) c->prefetch = -1;
   }

@@ -69,10 +69,7 @@ struct Params {
   int prefetch;           // bit 0: warm L2 with the first token's rows before
                           // waiting on the previous kernel; bit 1: also let the
                           // next kernel be scheduled at once; bit 2: while a
-                          // token is reduced, warm L2 with the next token's rows;
-                          // bit 3: before waiting, read one word of every
-                          // 128-byte line of the first token's rows (see
-                          // attnres_fused_kernel)
+                          // token is reduced, warm L2 with the next token's rows
 };
 
 // What a launch does with the prefix sum.
@@ -106,13 +103,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p)
                : "memory");
-  return r;
-}
-
-// One 32-bit word through L2 only (never allocated in L1).
-__device__ __forceinline__ uint32_t ld_l2_word(const void* p) {
-  uint32_t r;
-  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
   return r;
 }
 
@@ -953,27 +943,6 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // here, overlapping the previous kernel's tail (shared memory only); in the
   // streaming regime after the first token's loads are issued, so that the
   // set-up does not delay them.
-  // Latency regime, bit 3: read one 32-bit word of every 128-byte line of
-  // this CTA's first-token rows, through L2 only, before the wait.  On
-  // GB300 (two dies) lines that an SM has read are served to it faster than
-  // lines only prefetched into L2 (cold decode calls: 0.2-0.4 us faster);
-  // the values are discarded (consumed only by an empty asm after the
-  // wait), and no L1 line is allocated, so the loads after the wait see the
-  // previous kernel's writes.
-  constexpr int WROWS = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3);
-  constexpr bool WARM = (VPT == 1) && !HYB;
-  uint32_t warm[WARM ? WROWS : 1];
-#pragma unroll
-  for (int r = 0; r < (WARM ? WROWS : 1); ++r) warm[r] = 0;
-  if constexpr (WARM) {
-    if ((p.prefetch & 8) && blockIdx.y < p.M && ok[0] && (jj[0] & 7) == 0) {
-      const size_t off = static_cast<size_t>(blockIdx.y) * p.H8 + jj[0];
-#pragma unroll
-      for (int r = 0; r < WROWS; ++r)
-        warm[r] = ld_l2_word(r < N ? p.bank + r * p.bank_stride + off
-                             : r == N ? p.prefix + off : r == N + 1 ? p.add + off : p.add2 + off);
-    }
-  }
   const bool early_init = p.prefetch != 0;
   if (early_init && blockIdx.y < p.M) exchange_init<Sums<N>::total>(x, t, p);
   // Programmatic dependent launch: this grid may have been scheduled while
@@ -981,8 +950,6 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // complete (and its writes to be visible) before reading its outputs.
   // Without the launch attribute this returns at once.
   griddep_wait();
-#pragma unroll
-  for (int r = 0; r < (WARM ? WROWS : 1); ++r) asm volatile("" ::"r"(warm[r]));
 
   uint4 wv[VPT], gv[VPT];
 #pragma unroll
