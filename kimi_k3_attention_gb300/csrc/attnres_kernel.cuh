@@ -669,11 +669,15 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
   constexpr int S0 = S < 16 ? S : 16;  // sources of the first group
   const int lane = t.lane, warp = t.warp;
 
-  // ---- fold (the updated prefix is stored at the end: a global store in
-  // flight would make the release barriers below wait for it)
+  // ---- fold.  The latency shapes store the updated prefix at once, so that
+  // the store has drained by the end of the call; the streaming shapes
+  // store it at the end with the output (GB300: within noise there).
 #pragma unroll
-  for (int k = 0; k < VPT; ++k)
+  for (int k = 0; k < VPT; ++k) {
     src.set_new_prefix(k, MODE == kNoFold ? pr[k] : fold_chunk<MODE == kFoldAdd2, DT>(pr[k], ad[k], ad2[k]));
+    if constexpr (LAT && MODE != kNoFold)
+      if (ok[k]) st_out(p.new_prefix + row + jj[k], src.new_prefix(k));
+  }
 
   // ---- per-source sums of squares and dot products with w, and R1: warp
   // transpose-reduction per group, CTA sum, st.async to every CTA
@@ -850,7 +854,7 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     if (ok[k]) {
-      if (MODE != kNoFold) st_out(p.new_prefix + row + jj[k], src.new_prefix(k));
+      if (MODE != kNoFold && !LAT) st_out(p.new_prefix + row + jj[k], src.new_prefix(k));
       if (p.h_out != nullptr) {
         uint4 hv;
         hv.x = Fmt<DT>::pack(h[k][0], h[k][1]);
