@@ -170,9 +170,14 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *             its first token; 2 = let the next kernel be scheduled at once;
  *             4 = while a token is reduced, ask L2 for the CTA's rows of the
  *             next token it takes (when clusters walk several tokens);
- *             -1 = none; 0 = the default (1 up to 96 tokens, plus 4 when the
- *             grid is smaller than M).  A prefetch is a hint to a coherent L2
- *             and cannot change results.
+ *             8 = before waiting on the previous kernel, read one 32-bit
+ *             word of every 128-byte line of this CTA's rows of its first
+ *             token through L2 (values discarded, nothing allocated in L1):
+ *             lines an SM has read reach it sooner than lines only
+ *             prefetched; -1 = none; 0 = the default (1 up to 96 tokens, plus
+ *             8 up to 32 tokens, plus 4 when the grid is smaller than M).
+ *             These reads are hints to a coherent L2 and cannot change
+ *             results.
  */
 typedef struct {
   int variant;

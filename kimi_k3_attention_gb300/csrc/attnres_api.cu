@@ -266,11 +266,13 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c, bool bf1
   if (c->variant != 4) {
     if (c->stages != 0) return ATTNRES_ERR_CONFIG;
     if (c->grid_tokens == 0) {
-      // The register-capped shape runs best with about 14 clusters per SM
-      // in the grid, each walking a few tokens (GB300, M = 8192: 2128
-      // clusters, 5.6 TB/s, against 5.4 TB/s with one cluster per token and
-      // 3.7 TB/s with only the resident clusters, which fall into lock-step).
-      const long long cap = (c->variant == 3) ? 14LL * sms : 65535;
+      // The register-capped shape runs best with a grid of several clusters
+      // per SM, each walking a few tokens (GB300, M = 8192, N = 12: 9-11
+      // clusters per SM 6.40-6.42 TB/s, 14 per SM 6.36, 6 per SM 6.37, 3 per
+      // SM 6.20; one cluster per token was 5.4 TB/s and only the resident
+      // clusters 3.7 TB/s, falling into lock-step).  Deep banks keep 14 per
+      // SM, where their shapes were measured.
+      const long long cap = (c->variant == 3) ? (deep ? 14LL : 10LL) * sms : 65535;
       long long g = M < cap ? M : cap;
       c->grid_tokens = static_cast<int>(g < 65535 ? g : 65535);
     }
@@ -278,10 +280,11 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c, bool bf1
   }
   if (c->pdl < -1 || c->pdl > 1) return ATTNRES_ERR_CONFIG;
   if (c->pdl == 0) c->pdl = 1;
-  if (c->prefetch < -1 || c->prefetch > 7) return ATTNRES_ERR_CONFIG;
+  if (c->prefetch < -1 || c->prefetch > 15) return ATTNRES_ERR_CONFIG;
   if (c->prefetch == 0) {
     const bool fused = c->variant == 2 || c->variant == 3 || c->variant == 5;
     c->prefetch = (fused && M <= 96) ? 1 : 0;
+    if (fused && M <= 32) c->prefetch |= 8;   // the decode window
     if (fused && c->grid_tokens < M) c->prefetch |= 4;   // clusters walk tokens
     if (c->prefetch == 0) c->prefetch = -1;
   }

@@ -385,7 +385,7 @@ def test_pipe_invalid_stages_rejected():
         assert e.value.status == -8
 
 
-@pytest.mark.parametrize("prefetch", [-1, 1, 2, 3, 4, 5, 7])
+@pytest.mark.parametrize("prefetch", [-1, 1, 2, 3, 4, 5, 7, 8, 9, 15])
 def test_prefetch_modes_identical(prefetch):
     """L2 prefetch and early dependent launch change scheduling only; a
     dependent chain queued without host synchronisation stays exact."""
