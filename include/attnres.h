@@ -155,8 +155,21 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *   threads   threads per CTA, a multiple of 32 within the variant's limit;
  *             0 = the smallest count that covers the CTA's columns.
  *   grid_tokens  CTAs (clusters) along the token axis, each looping over
- *             tokens with this stride; 0 = min(M, 65535), or for variant 4
- *             the number of clusters that can be resident at once.
+ *             tokens with this stride (see tail_tokens); 0 = sized when the
+ *             kernel is launched for variants 3 and 4 (below), else
+ *             min(M, 65535).  Variant 4: the clusters that fit the GPU at
+ *             once.  Variant 3: with R clusters fitting at once, about
+ *             sqrt(2M/R) + R sqrt(M/(2R)) clusters: the walking ones take
+ *             about L = sqrt(2M/R) tokens each, the last R L / 2 one token
+ *             each (clusters start in grid order, so the short ones fill
+ *             the SMs that the walks leave idle at the end); with M below
+ *             about R, one cluster per token.
+ *   tail_tokens  variants 1, 2, 3 and 5 with grid_tokens > 0: the last
+ *             tail_tokens clusters of the grid take one token each (the last
+ *             tail_tokens tokens) and the other grid_tokens - tail_tokens
+ *             walk the rest with that stride; needs tail_tokens <
+ *             grid_tokens <= M.  0 = none (and chosen with the grid when
+ *             grid_tokens is 0).  Must be 0 for variant 4.
  *   pdl       programmatic dependent launch: 1 = on, -1 = off, 0 = the
  *             default (on).  With it the kernel may be scheduled while the
  *             previous kernel on the stream is still running; it waits for
@@ -187,6 +200,7 @@ typedef struct {
   int pdl;
   int stages;
   int prefetch;
+  int tail_tokens;
 } attnres_config;
 
 /* The fused epilogue with a pinned configuration (cfg may be NULL = auto).
@@ -301,8 +315,8 @@ int attnres_launch(const attnres_args* args, const attnres_config* cfg,
 
 /* The configuration attnres_add_rmsnorm would launch for (M, N, H) with
  * (has_add2 != 0) or without a second addend on the current device, written
- * to *plan with every field resolved (grid_tokens 0 for variant 4 means
- * "as many clusters as fit").  Returns a status; needs a CUDA device (it
+ * to *plan with every field resolved (grid_tokens 0 for variants 3 and 4:
+ * sized from the clusters that fit when the kernel is launched).  Returns a status; needs a CUDA device (it
  * reads the SM count). */
 int attnres_plan(int M, int N, int H, int has_add2, attnres_config* plan);
 

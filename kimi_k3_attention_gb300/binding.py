@@ -52,7 +52,8 @@ class AttnResError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("cluster", ctypes.c_int),
                 ("threads", ctypes.c_int), ("grid_tokens", ctypes.c_int), ("pdl", ctypes.c_int),
-                ("stages", ctypes.c_int), ("prefetch", ctypes.c_int)]
+                ("stages", ctypes.c_int), ("prefetch", ctypes.c_int),
+                ("tail_tokens", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -140,10 +141,10 @@ def _stream_handle(stream):
 
 
 def make_config(variant="auto", cluster=0, threads=0, grid_tokens=0, pdl=0, stages=0,
-                prefetch=0) -> Config:
+                prefetch=0, tail_tokens=0) -> Config:
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     return Config(v, int(cluster), int(threads), int(grid_tokens), int(pdl), int(stages),
-                  int(prefetch))
+                  int(prefetch), int(tail_tokens))
 
 
 def _dtype_code(t) -> int:

@@ -260,23 +260,27 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c, bool bf1
     // grid_tokens 0 stays 0: the launcher sizes the grid to the resident
     // clusters.
     if (c->grid_tokens < 0 || c->grid_tokens > 65535) return ATTNRES_ERR_CONFIG;
+    if (c->tail_tokens != 0) return ATTNRES_ERR_CONFIG;
   } else {
     return ATTNRES_ERR_CONFIG;
   }
   if (c->variant != 4) {
     if (c->stages != 0) return ATTNRES_ERR_CONFIG;
+    if (c->tail_tokens < 0) return ATTNRES_ERR_CONFIG;
+    // The register-capped shapes (variant 3) keep grid_tokens 0: the launcher
+    // sizes a walk from the clusters that fit at once (walk_grid; with M
+    // below about R, one cluster per token).  GB300, M = 8192, N = 12,
+    // against grids of clusters that each walk an equal share: 10 per SM
+    // 6.44 TB/s, 6 or 14 per SM 6.37, only the resident clusters 3.7.
+    if (c->grid_tokens == 0 && c->variant != 3) c->grid_tokens = M < 65535 ? M : 65535;
     if (c->grid_tokens == 0) {
-      // The register-capped shape runs best with a grid of several clusters
-      // per SM, each walking a few tokens (GB300, M = 8192, N = 12: 9-11
-      // clusters per SM 6.40-6.42 TB/s, 14 per SM 6.36, 6 per SM 6.37, 3 per
-      // SM 6.20; one cluster per token was 5.4 TB/s and only the resident
-      // clusters 3.7 TB/s, falling into lock-step).  Deep banks keep 14 per
-      // SM, where their shapes were measured.
-      const long long cap = (c->variant == 3) ? (deep ? 14LL : 10LL) * sms : 65535;
-      long long g = M < cap ? M : cap;
-      c->grid_tokens = static_cast<int>(g < 65535 ? g : 65535);
+      if (c->tail_tokens != 0) return ATTNRES_ERR_CONFIG;
+    } else {
+      if (c->grid_tokens < 1 || c->grid_tokens > 65535) return ATTNRES_ERR_CONFIG;
+      // the walking clusters need a token each
+      if (c->tail_tokens > 0 && (c->tail_tokens >= c->grid_tokens || c->grid_tokens > M))
+        return ATTNRES_ERR_CONFIG;
     }
-    if (c->grid_tokens < 1 || c->grid_tokens > 65535) return ATTNRES_ERR_CONFIG;
   }
   if (c->pdl < -1 || c->pdl > 1) return ATTNRES_ERR_CONFIG;
   if (c->pdl == 0) c->pdl = 1;
@@ -298,8 +302,10 @@ cudaError_t dispatch(int N, bool add2, const Params& p, dim3 g, int t, int c, bo
                      cudaStream_t s) {
 #define ATTNRES_CASE(n)                                                                  \
   case n:                                                                                \
-    return add2 ? launch_fused<n, kFoldAdd2, VPT, MAXT, MINB>(p, g, t, c, pdl, s)        \
-                : launch_fused<n, kFoldAdd, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
+    return add2 ? launch_fused<n, kFoldAdd2, VPT, MAXT, minb_of(MINB, n, kFoldAdd2)>(      \
+                      p, g, t, c, pdl, s)                                                 \
+                : launch_fused<n, kFoldAdd, VPT, MAXT, minb_of(MINB, n, kFoldAdd)>(        \
+                      p, g, t, c, pdl, s);
   switch (N) {
     ATTNRES_CASE(0)
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
@@ -316,7 +322,7 @@ cudaError_t dispatch_nofold(int N, const Params& p, dim3 g, int t, int c, bool p
                             cudaStream_t s) {
 #define ATTNRES_CASE(n) \
   case n:               \
-    return launch_fused<n, kNoFold, VPT, MAXT, MINB>(p, g, t, c, pdl, s);
+    return launch_fused<n, kNoFold, VPT, MAXT, minb_of(MINB, n, kNoFold)>(p, g, t, c, pdl, s);
   switch (N) {
     ATTNRES_CASE(0)
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
@@ -346,9 +352,12 @@ cudaError_t dispatch_fp16(int N, int mode, const Params& p, dim3 g, int t, int c
 #define ATTNRES_CASE(n)                                                                    \
   case n:                                                                                  \
     return mode == kFoldAdd2                                                               \
-               ? launch_fused<n, kFoldAdd2, VPT, MAXT, MINB, kFP16>(p, g, t, c, pdl, s)    \
-           : mode == kFoldAdd ? launch_fused<n, kFoldAdd, VPT, MAXT, MINB, kFP16>(p, g, t, c, pdl, s) \
-                              : launch_fused<n, kNoFold, VPT, MAXT, MINB, kFP16>(p, g, t, c, pdl, s);
+               ? launch_fused<n, kFoldAdd2, VPT, MAXT, minb_of(MINB, n, kFoldAdd2), kFP16>(   \
+                     p, g, t, c, pdl, s)                                                   \
+           : mode == kFoldAdd                                                              \
+               ? launch_fused<n, kFoldAdd, VPT, MAXT, minb_of(MINB, n, kFoldAdd), kFP16>(     \
+                     p, g, t, c, pdl, s)                                                   \
+               : launch_fused<n, kNoFold, VPT, MAXT, minb_of(MINB, n, kNoFold), kFP16>(p, g, t, c, pdl, s);
   switch (N) {
     ATTNRES_CASE(0)
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
@@ -415,7 +424,7 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   int sms = 0;
   if ((st = current_device(&sms)) != ATTNRES_OK) return st;
   const bool has_add2 = a.fold && a.add2 != nullptr;
-  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0, 0, 0};
+  attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0, 0, 0, 0};
   if ((st = resolve(a.M, a.N, has_add2, a.H, sms, &c, a.fold && a.dtype == ATTNRES_DTYPE_BF16)) !=
       ATTNRES_OK)
     return st;
@@ -444,6 +453,7 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   p.wait_ns = static_cast<unsigned long long>(g_wait_ns.load(std::memory_order_relaxed));
   p.extra_tx = g_extra_tx.load(std::memory_order_relaxed);
   p.prefetch = c.prefetch > 0 ? c.prefetch : 0;
+  p.tail = c.tail_tokens;   // grid_tokens 0: set by the launcher
 
   const dim3 grid(static_cast<unsigned>(c.cluster), static_cast<unsigned>(c.grid_tokens), 1);
   const bool pdl = c.pdl >= 0;
@@ -644,7 +654,7 @@ extern "C" int attnres_access_pattern(const void* prefix, const void* add, const
   if (st != ATTNRES_OK) return st;
   int sms = 0;
   if ((st = current_device(&sms)) != ATTNRES_OK) return st;
-  attnres_config c = {0, 0, 0, 0, 0, 0, 0};
+  attnres_config c = {0, 0, 0, 0, 0, 0, 0, 0};
   if ((st = resolve(M, N, true, H, sms, &c, true)) != ATTNRES_OK) return st;
   if (c.threads > kPatternMaxT) return ATTNRES_ERR_CONFIG;
   Params p = {};
@@ -672,7 +682,7 @@ extern "C" int attnres_plan(int M, int N, int H, int has_add2, attnres_config* p
   int sms = 0;
   int st = current_device(&sms);
   if (st != ATTNRES_OK) return st;
-  attnres_config c = {0, 0, 0, 0, 0, 0, 0};
+  attnres_config c = {0, 0, 0, 0, 0, 0, 0, 0};
   if ((st = resolve(M, N, has_add2 != 0, H, sms, &c, true)) != ATTNRES_OK) return st;
   *plan = c;
   return ATTNRES_OK;
@@ -719,4 +729,4 @@ extern "C" int attnres_debug_exchange(int extra_bytes, long long wait_ns) {
   return ATTNRES_OK;
 }
 
-extern "C" int attnres_version(void) { return 100; }
+extern "C" int attnres_version(void) { return 200; }

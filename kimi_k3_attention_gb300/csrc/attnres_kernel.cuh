@@ -72,6 +72,30 @@ struct Params {
                           // token is reduced, warm L2 with the next token's rows;
                           // bit 3: before waiting, read a word of every 128-byte
                           // line of the first token's rows
+  int tail;               // the last `tail` clusters of the grid take one
+                          // token each (see TokenWalk); 0 = none
+  int walkers;            // set by the launcher: gridDim.y - tail
+  int walk_end;           // set by the launcher: M - tail
+};
+
+// The tokens one cluster handles.  With tail == 0, cluster c takes c,
+// c + G, c + 2G, ... (G = gridDim.y).  With tail = T > 0 the first G - T
+// clusters walk tokens [0, M - T) with stride G - T and the last T clusters
+// take one token each, M - T + (c - (G - T)): clusters are started in grid
+// order, so the short ones come last and fill the SMs that the long walks
+// leave idle at the end.  The host keeps 0 <= T < G <= M.  Written with the
+// launch parameters only, so that the walk holds no registers beyond the
+// token index.
+struct TokenWalk {
+  static __device__ __forceinline__ int first(const Params& p) {
+    const int c = static_cast<int>(blockIdx.y);
+    return c < p.walkers ? c : p.walk_end + (c - p.walkers);
+  }
+  // the token this cluster takes after m, or M when it has none
+  static __device__ __forceinline__ int next(const Params& p, int m) {
+    const int n = m + p.walkers;
+    return (m < p.walk_end && n < p.walk_end) ? n : p.M;
+  }
 };
 
 // What a launch does with the prefix sum.
@@ -906,8 +930,8 @@ __device__ __forceinline__ Thread thread_info() {
 
 // ---------------------------------------------------------------- kernels
 
-// Loads straight to registers; each cluster handles tokens blockIdx.y,
-// blockIdx.y + gridDim.y, ...  DT is the element format of every tensor.
+// Loads straight to registers; each cluster handles the tokens of its
+// TokenWalk.  DT is the element format of every tensor.
 // NR < N keeps bank rows NR..N-1 in shared memory instead (HybridSources;
 // one column chunk per thread).
 template <int N, int MODE, int VPT, int MAXT, int MINB, int DT = kBF16, int NR = N>
@@ -920,6 +944,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   __shared__ Exchange<Sums<N>::G> x;
   extern __shared__ __align__(16) uint4 hyb[];   // [N - NR][blockDim.x] when HYB
   Thread t = thread_info();
+  const int m0 = TokenWalk::first(p);
   const int c0 = static_cast<int>(t.crank) * p.cpc;
   const int cend = min(c0 + p.cpc, p.H8);
   int jj[VPT];
@@ -938,9 +963,9 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   if (p.prefetch & 1) {
     const int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3) + 2;
     // (a hint: with fewer threads than rows, the last rows go without)
-    if (static_cast<int>(threadIdx.x) < rows && cend > c0 && blockIdx.y < p.M) {
+    if (static_cast<int>(threadIdx.x) < rows && cend > c0 && m0 < p.M) {
       const int r = threadIdx.x;
-      const size_t off = static_cast<size_t>(blockIdx.y) * p.H8 + c0;
+      const size_t off = static_cast<size_t>(m0) * p.H8 + c0;
       const uint32_t bytes = static_cast<uint32_t>(cend - c0) * 16u;
       const uint4* src = r < N ? p.bank + r * p.bank_stride + off
                        : r == N ? p.prefix + off
@@ -957,7 +982,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // streaming regime after the first token's loads are issued, so that the
   // set-up does not delay them.
   const bool early_init = p.prefetch != 0;
-  if (early_init && blockIdx.y < p.M) exchange_init<Sums<N>::total>(x, t, p);
+  if (early_init && m0 < p.M) exchange_init<Sums<N>::total>(x, t, p);
   // Latency regime, bit 3: before the wait, read one 32-bit word of every
   // 128-byte line of this CTA's first-token rows (through L2 only, never
   // allocated in L1).  On GB300 lines an SM has read are served to it faster
@@ -968,8 +993,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // past it); a test that can never be true keeps them.  The values are
   // discarded, and the loads after the wait see the previous kernel's writes.
   if constexpr (VPT == 1 && !HYB) {
-    if ((p.prefetch & 8) && blockIdx.y < p.M && ok[0] && (jj[0] & 7) == 0) {
-      const size_t off = static_cast<size_t>(blockIdx.y) * p.H8 + jj[0];
+    if ((p.prefetch & 8) && m0 < p.M && ok[0] && (jj[0] & 7) == 0) {
+      const size_t off = static_cast<size_t>(m0) * p.H8 + jj[0];
       constexpr int WROWS = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3);
       uint32_t acc = 0;
 #pragma unroll
@@ -993,7 +1018,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   }
 
   bool first = true;
-  for (int m = blockIdx.y; m < p.M; m += gridDim.y) {
+  for (int m = m0; m < p.M; m = TokenWalk::next(p, m)) {
     const size_t row = static_cast<size_t>(m) * p.H8;
     uint4 v[NR + 1][VPT];
     uint4 pr[VPT], ad[VPT], ad2[VPT];
@@ -1020,11 +1045,11 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // While this token is reduced, let L2 fetch this CTA's rows of the next
     // token it will take: the requests keep HBM busy during the reductions
     // and the next loads hit L2.
-    if ((p.prefetch & 4) && m + static_cast<int>(gridDim.y) < p.M) {
+    if ((p.prefetch & 4) && TokenWalk::next(p, m) < p.M) {
       constexpr int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3);
       if (static_cast<int>(threadIdx.x) < rows && cend > c0) {
         const int r = threadIdx.x;
-        const size_t off = static_cast<size_t>(m + gridDim.y) * p.H8 + c0;
+        const size_t off = static_cast<size_t>(TokenWalk::next(p, m)) * p.H8 + c0;
         const uint4* src = r < N ? p.bank + r * p.bank_stride + off
                          : r == N ? p.prefix + off
                          : r == N + 1 ? p.add + off : p.add2 + off;
@@ -1033,8 +1058,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     }
     // Let the next kernel on the stream be scheduled once every CTA of this
     // grid is past its first loads; it still waits for this grid to finish.
-    if (m == static_cast<int>(blockIdx.y)) griddep_launch_dependents();
-    if (!early_init && m == static_cast<int>(blockIdx.y)) exchange_init<Sums<N>::total>(x, t, p);
+    if (m == m0) griddep_launch_dependents();
+    if (!early_init && m == m0) exchange_init<Sums<N>::total>(x, t, p);
     if constexpr (HYB) {
       cp_async_wait<0>();   // this thread's own slots: no barrier needed
       HybridSources<N, NR> src{v, hyb0, hstep, ok[0]};
@@ -1162,7 +1187,7 @@ __global__ void __launch_bounds__(kPatternMaxT) attnres_pattern_kernel(const Par
   const int j = c0 + static_cast<int>(threadIdx.x);
   const bool ok = j < cend;
   griddep_wait();
-  for (int m = blockIdx.y; m < p.M; m += gridDim.y) {
+  for (int m = TokenWalk::first(p); m < p.M; m = TokenWalk::next(p, m)) {
     const size_t row = static_cast<size_t>(m) * p.H8;
     uint4 v[N + 3];
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -1171,11 +1196,11 @@ __global__ void __launch_bounds__(kPatternMaxT) attnres_pattern_kernel(const Par
     v[2] = ok ? ld_stream(p.add2 + row + j) : z;
 #pragma unroll
     for (int i = 0; i < N; ++i) v[3 + i] = ok ? ld_stream(p.bank + i * p.bank_stride + row + j) : z;
-    if ((p.prefetch & 4) && m + static_cast<int>(gridDim.y) < p.M) {
+    if ((p.prefetch & 4) && TokenWalk::next(p, m) < p.M) {
       constexpr int rows = N + 3;
       if (static_cast<int>(threadIdx.x) < rows && cend > c0) {
         const int r = threadIdx.x;
-        const size_t off = static_cast<size_t>(m + gridDim.y) * p.H8 + c0;
+        const size_t off = static_cast<size_t>(TokenWalk::next(p, m)) * p.H8 + c0;
         const uint4* src = r < N ? p.bank + r * p.bank_stride + off
                          : r == N ? p.prefix + off : r == N + 1 ? p.add + off : p.add2 + off;
         prefetch_l2(src, static_cast<uint32_t>(cend - c0) * 16u);

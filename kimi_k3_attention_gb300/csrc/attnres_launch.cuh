@@ -3,6 +3,7 @@
 #pragma once
 
 #include <atomic>
+#include <cmath>
 
 #include "attnres_kernel.cuh"
 
@@ -13,15 +14,28 @@ constexpr int kMaxDevices = 64;
 // The compiled shapes of the kernel.
 //   split:  8 columns per thread, up to 256 threads (a cluster of CTAs per token)
 //   stream: 8 columns per thread, up to 224 threads, registers capped so
-//           that three CTAs fit an SM (many tokens in flight at large M);
-//           deep banks have their own streaming shape (below)
+//           that several CTAs fit an SM (many tokens in flight at large M;
+//           stream_minb); deep banks have their own streaming shape (below)
 //   cta:    16 columns per thread, up to 448 threads (one CTA per token)
 constexpr int kSplitVPT = 1, kSplitMaxT = 256, kSplitMinB = 1;
 // split2: the split shape with registers capped so that two CTAs of up to
 // 256 threads share an SM (the next call's CTAs can be resident while this
 // call runs, under programmatic dependent launch)
 constexpr int kSplit2MinB = 2;
-constexpr int kStreamVPT = 1, kStreamMaxT = 224, kStreamMinB = 3;
+constexpr int kStreamVPT = 1, kStreamMaxT = 224;
+// The streaming shape's registers: capped at 72 (four CTAs of 224 threads,
+// or seven of 128, per SM) while a token has at most 12 rows (bank, prefix
+// and addends: N <= 9 with add2), which then fit without spilling, else at
+// 80 (three of 224, six of 128).  GB300, M = 8192, add2, the cap of 72
+// against 80: N = 2, 5..9 +2..8 %, N = 1, 3, 4 within 1 %; N = 10..12
+// (12-42 spilled bytes) -1..-9 %.
+constexpr int stream_rows(int n, int mode) {
+  return n + (mode == kFoldAdd2 ? 3 : mode == kFoldAdd ? 2 : 1);
+}
+constexpr int stream_minb(int n, int mode) { return stream_rows(n, mode) <= 12 ? 4 : 3; }
+// Dispatch's MINB for the streaming shape: stream_minb of each (N, mode).
+constexpr int kStreamMinB = 0;
+constexpr int minb_of(int minb, int n, int mode) { return minb != 0 ? minb : stream_minb(n, mode); }
 constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 
 // Every shape is compiled for N <= kShallowMaxN.  Deeper banks (up to
@@ -35,6 +49,64 @@ constexpr int kShallowMaxN = 12;
 constexpr int kDeepStreamMaxT = 128;
 constexpr int deep_minb(int n) { return n <= 16 ? 5 : 4; }
 constexpr int deep_nr(int n) { return n >= 23 ? 16 : n; }
+
+// Clusters that fit the device at once for launch configuration cfg (its
+// block size, dynamic shared memory and cluster attribute), cached per
+// device for the last (threads, cluster, shared memory) asked.
+template <class Kern>
+cudaError_t resident_clusters(Kern kern, cudaLaunchConfig_t cfg, int dev, int cluster,
+                              std::atomic<long long>* cache, int* clusters) {
+  const long long key = (static_cast<long long>(cfg.blockDim.x) << 8 | cluster) << 20 |
+                        static_cast<long long>(cfg.dynamicSmemBytes >> 4);
+  const long long c = cache[dev].load(std::memory_order_acquire);
+  if (c != 0 && (c >> 16) == key) {
+    *clusters = static_cast<int>(c & 0xffff);
+    return cudaSuccess;
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  if (n > 0xffff) n = 0xffff;
+  cache[dev].store(key << 16 | n, std::memory_order_release);
+  *clusters = n;
+  return cudaSuccess;
+}
+
+// The automatic grid of a walk over M tokens when R clusters fit the GPU at
+// once (grid_tokens 0 for the streaming shapes).  Walking clusters take about
+// L = sqrt(2 M / R) tokens each and the last T = R L / 2 clusters one token
+// each (TokenWalk).  Clusters start in grid order as slots free up, so the
+// walks end spread over about L tokens' time, and the T one-token clusters,
+// started last, fill the slots that finish early.  Every cluster costs a
+// start (its first token is not prefetched): L minimises the clusters per
+// slot, M / (L R) + L / 2.  GB300, N = 12, against 10 clusters per SM each
+// walking an equal share: +2 % at M = 8192 and 16384, +5 % at M = 4096,
+// every cell of a sweep of (M - T) / L and T around this choice within 1 %
+// of the best.  L < 2: one cluster per token.
+inline void walk_grid(int M, int R, unsigned* gy, int* tail) {
+  const long long L = std::llround(std::sqrt(2.0 * M / (R > 0 ? R : 1)));
+  if (L < 2) {
+    *gy = static_cast<unsigned>(M < 65535 ? M : 65535);
+    *tail = 0;
+    return;
+  }
+  long long T = (static_cast<long long>(R) * L + 1) / 2;
+  if (T > M / 2) T = M / 2;
+  if (T > 32767) T = 32767;
+  long long walkers = (M - T + L - 1) / L;
+  if (walkers + T > 65535) walkers = 65535 - T;
+  *gy = static_cast<unsigned>(walkers + T);
+  *tail = static_cast<int>(T);
+}
+
+// The launch parameters of TokenWalk for a grid of gy clusters (p.tail set,
+// 0 <= tail < gy <= M when tail > 0).
+inline void set_walk(Params& p, unsigned gy) {
+  p.walkers = static_cast<int>(gy) - p.tail;
+  p.walk_end = p.M - p.tail;
+}
 
 template <int N, int MODE, int VPT, int MAXT, int MINB, int DT, int NR>
 cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, bool pdl,
@@ -77,7 +149,21 @@ cudaError_t launch_fused(const Params& p, dim3 grid, int threads, int cluster, b
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  Params q = p;
+  if (grid.y == 0) {
+    // size the walk from the clusters that fit at once
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    static std::atomic<long long> cache[kMaxDevices];
+    int clusters = 0;
+    e = resident_clusters(kern, cfg, dev, cluster, cache, &clusters);
+    if (e != cudaSuccess) return e;
+    walk_grid(p.M, clusters, &cfg.gridDim.y, &q.tail);
+  }
+  set_walk(q, cfg.gridDim.y);
+  return cudaLaunchKernelEx(&cfg, kern, q);
 }
 
 // The persistent pipelined kernel: up to 256 threads, STAGES tokens in the
@@ -129,22 +215,10 @@ cudaError_t launch_pipe(const Params& p, dim3 grid, int threads, int cluster, bo
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
   if (grid.y == 0) {
-    // Resident clusters for this (threads, cluster, shared memory), cached
-    // per device for the last configuration asked.
     static std::atomic<long long> cache[kMaxDevices];
-    const long long key = (static_cast<long long>(threads) << 8 | cluster) << 20 | static_cast<long long>(smem >> 4);
-    long long c = cache[dev].load(std::memory_order_acquire);
     int clusters = 0;
-    if (c != 0 && (c >> 16) == key) {
-      clusters = static_cast<int>(c & 0xffff);
-    } else {
-      cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
-      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-      if (e != cudaSuccess) return e;
-      if (clusters < 1) return cudaErrorInvalidConfiguration;
-      if (clusters > 0xffff) clusters = 0xffff;
-      cache[dev].store(key << 16 | clusters, std::memory_order_release);
-    }
+    e = resident_clusters(kern, cfg, dev, cluster, cache, &clusters);
+    if (e != cudaSuccess) return e;
     grid.y = static_cast<unsigned>(clusters < p.M ? clusters : p.M);
   }
   if (grid.y > 65535u) grid.y = 65535u;
@@ -203,7 +277,21 @@ cudaError_t launch_pattern(const Params& p, dim3 grid, int threads, int cluster,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  Params q = p;
+  if (grid.y == 0) {
+    // the fused kernel's automatic walk, sized for this kernel
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    static std::atomic<long long> cache[kMaxDevices];
+    int clusters = 0;
+    e = resident_clusters(kern, cfg, dev, cluster, cache, &clusters);
+    if (e != cudaSuccess) return e;
+    walk_grid(p.M, clusters, &cfg.gridDim.y, &q.tail);
+  }
+  set_walk(q, cfg.gridDim.y);
+  return cudaLaunchKernelEx(&cfg, kern, q);
 }
 
 // Instantiations.  Each attnres_inst_*.cu unit expands its share with DEF
@@ -230,7 +318,8 @@ cudaError_t launch_pattern(const Params& p, dim3 grid, int threads, int cluster,
 #define ATTNRES_INSTANTIATE(DEF, N, ADD2)                                                   \
   ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB)     \
   ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kSplitVPT, kSplitMaxT, kSplit2MinB)    \
-  ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kStreamVPT, kStreamMaxT, kStreamMinB)  \
+  ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kStreamVPT, kStreamMaxT,              \
+                stream_minb(N, ADD2 ? kFoldAdd2 : kFoldAdd))                                \
   ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kCtaVPT, kCtaMaxT, kCtaMinB)           \
   ATTNRES_PIPE(DEF, N, ADD2, 2)                                                             \
   ATTNRES_PIPE(DEF, N, ADD2, 3)                                                             \
@@ -240,7 +329,7 @@ cudaError_t launch_pattern(const Params& p, dim3 grid, int threads, int cluster,
 // streaming shapes.
 #define ATTNRES_INSTANTIATE_NOFOLD(DEF, N)                               \
   ATTNRES_FUSED(DEF, N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB)      \
-  ATTNRES_FUSED(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, kStreamMinB)
+  ATTNRES_FUSED(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, stream_minb(N, kNoFold))
 
 // Deep banks, 13 <= N <= 31: the split shape and the deep streaming shape,
 // with the fold (add2 present or not) and without, for element format DT.
@@ -260,9 +349,9 @@ cudaError_t launch_pattern(const Params& p, dim3 grid, int threads, int cluster,
   ATTNRES_FUSED_DT(DEF, N, kFoldAdd2, kSplitVPT, kSplitMaxT, kSplitMinB, kFP16)        \
   ATTNRES_FUSED_DT(DEF, N, kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB, kFP16)         \
   ATTNRES_FUSED_DT(DEF, N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB, kFP16)          \
-  ATTNRES_FUSED_DT(DEF, N, kFoldAdd2, kStreamVPT, kStreamMaxT, kStreamMinB, kFP16)     \
-  ATTNRES_FUSED_DT(DEF, N, kFoldAdd, kStreamVPT, kStreamMaxT, kStreamMinB, kFP16)      \
-  ATTNRES_FUSED_DT(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, kStreamMinB, kFP16)
+  ATTNRES_FUSED_DT(DEF, N, kFoldAdd2, kStreamVPT, kStreamMaxT, stream_minb(N, kFoldAdd2), kFP16) \
+  ATTNRES_FUSED_DT(DEF, N, kFoldAdd, kStreamVPT, kStreamMaxT, stream_minb(N, kFoldAdd), kFP16)   \
+  ATTNRES_FUSED_DT(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, stream_minb(N, kNoFold), kFP16)
 
 #define ATTNRES_TAIL_ADD(DEF, ADD2, DT)                                                      \
   DEF template cudaError_t launch_tail_add<ADD2, DT>(const uint4*, const uint4*, const uint4*,  \

@@ -93,9 +93,9 @@ def test_alias_rules():
 
 def test_config_struct_layout():
     c = binding.make_config("cluster", cluster=8, threads=128)
-    assert ctypes.sizeof(c) == 28
+    assert ctypes.sizeof(c) == 32
     assert c.as_dict() == {"variant": 2, "cluster": 8, "threads": 128, "grid_tokens": 0, "pdl": 0,
-                           "stages": 0, "prefetch": 0}
+                           "stages": 0, "prefetch": 0, "tail_tokens": 0}
 
 
 def test_new_entry_points_validate_on_host():

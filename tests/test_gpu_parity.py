@@ -243,6 +243,49 @@ def test_token_loop(grid_tokens):
     assert_parity(inp, gnp, gout)
 
 
+@pytest.mark.parametrize("grid_tokens,tail_tokens", [(2, 1), (10, 4), (67, 66), (40, 39), (67, 1)])
+def test_tail_tokens(grid_tokens, tail_tokens):
+    """The last tail_tokens clusters take one token each, the others walk the
+    rest: every token once, the same bits as one cluster per token."""
+    inp = wl.make_inputs(67, 6, H, seed=13)
+    for variant, cl in (("cluster", 4), ("stream", 7), ("stream", 4), ("cluster2", 8), ("cta", 0)):
+        plain = binding.make_config(variant, cluster=cl, grid_tokens=67)
+        walk = binding.make_config(variant, cluster=cl, grid_tokens=grid_tokens,
+                                   tail_tokens=tail_tokens)
+        rnp, rout = run_gpu(inp, plain)
+        gnp, gout = run_gpu(inp, walk)
+        assert (gnp == rnp).all() and (gout == rout).all(), (variant, cl)
+        assert_parity(inp, gnp, gout, label=f"{variant}{cl}")
+
+
+@pytest.mark.parametrize("M,N", [(300, 3), (1200, 12), (2500, 1)])
+def test_automatic_walk(M, N):
+    """Register-capped shape with the launch-time grid (walking clusters and
+    one-token clusters at the end): the same bits as one cluster per token."""
+    inp = wl.make_inputs(M, N, H, seed=14 + M, add2=True)
+    plan = binding.attnres_plan(M, N, H)
+    assert plan["variant"] == 3 and plan["grid_tokens"] == 0 and plan["tail_tokens"] == 0
+    gnp, gout = run_gpu(inp)
+    rnp, rout = run_gpu(inp, binding.make_config("stream", cluster=plan["cluster"], grid_tokens=M))
+    assert (gnp == rnp).all() and (gout == rout).all()
+    toks = np.unique(np.linspace(0, M - 1, 64).astype(int))
+    assert_parity(inp, gnp, gout, tokens=toks)
+
+
+def test_tail_tokens_rejected():
+    inp = wl.make_inputs(9, 2, H, seed=15).to("cuda")
+    out, np_ = torch.empty_like(inp.prefix), torch.empty_like(inp.prefix)
+    def call(cfg):
+        with pytest.raises(binding.AttnResError):
+            binding.attnres_add_rmsnorm(inp.prefix, inp.add, inp.add2, inp.bank, inp.w, inp.gamma,
+                                        inp.eps, out, np_, config=cfg)
+    call(binding.make_config("stream", cluster=4, grid_tokens=4, tail_tokens=4))    # no walker
+    call(binding.make_config("stream", cluster=4, grid_tokens=10, tail_tokens=2))   # grid > M
+    call(binding.make_config("stream", cluster=4, tail_tokens=2))                   # auto grid
+    call(binding.make_config("stream", cluster=4, grid_tokens=4, tail_tokens=-1))
+    call(binding.make_config("pipe", cluster=4, grid_tokens=4, tail_tokens=1))
+
+
 def test_more_tokens_than_grid_limit():
     """M above 65535: the grid's token axis is capped and clusters loop."""
     M, Hs = 70000, 64
