@@ -132,7 +132,9 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *                 per thread (<= 256 threads); the per-token sums are
  *                 exchanged through distributed shared memory;
  *             3 = as 2 with at most 224 threads and registers capped so that
- *                 three CTAs share an SM;
+ *                 three CTAs share an SM (four while a token has at most 12
+ *                 rows: N <= 9 with add2, N <= 10 without, N <= 11
+ *                 without the fold);
  *             5 = as 2 with registers capped so that two CTAs of up to 256
  *                 threads share an SM (in back-to-back calls the next
  *                 call's CTAs can become resident, and prefetch, while this
@@ -141,8 +143,9 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *             Variants 1, 4 and 5 exist for N <= 12 only (variant 5 with
  *             the fold on BF16 tensors only).  For N > 12
  *             variant 3 takes at most 128 threads, registers capped so
- *             that four or five CTAs share an SM (from N = 23 on with
- *             bank rows 16..N-1 in dynamic shared memory).
+ *             that four to seven CTAs share an SM (at N = 16 with bank
+ *             rows 8..15, from N = 23 on with rows 16..N-1, in dynamic
+ *             shared memory).
  *             4 = persistent and pipelined (the large-M streaming kernel): a
  *                 grid of as many clusters as fit the GPU at once walks the
  *                 tokens; every thread copies its chunks of the token
@@ -164,12 +167,12 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *             each (clusters start in grid order, so the short ones fill
  *             the SMs that the walks leave idle at the end); with M below
  *             about R, one cluster per token.
- *   tail_tokens  variants 1, 2, 3 and 5 with grid_tokens > 0: the last
- *             tail_tokens clusters of the grid take one token each (the last
- *             tail_tokens tokens) and the other grid_tokens - tail_tokens
- *             walk the rest with that stride; needs tail_tokens <
- *             grid_tokens <= M.  0 = none (and chosen with the grid when
- *             grid_tokens is 0).  Must be 0 for variant 4.
+ *   tail_tokens  variant 3 with grid_tokens > 0: the last tail_tokens
+ *             clusters of the grid take one token each (the last tail_tokens
+ *             tokens) and the other grid_tokens - tail_tokens walk the rest
+ *             with that stride; needs tail_tokens < grid_tokens <= M.  0 =
+ *             none (and chosen with the grid when grid_tokens is 0).  Must
+ *             be 0 for the other variants.
  *   pdl       programmatic dependent launch: 1 = on, -1 = off, 0 = the
  *             default (on).  With it the kernel may be scheduled while the
  *             previous kernel on the stream is still running; it waits for

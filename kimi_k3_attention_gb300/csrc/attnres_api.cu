@@ -277,8 +277,9 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c, bool bf1
       if (c->tail_tokens != 0) return ATTNRES_ERR_CONFIG;
     } else {
       if (c->grid_tokens < 1 || c->grid_tokens > 65535) return ATTNRES_ERR_CONFIG;
-      // the walking clusters need a token each
-      if (c->tail_tokens > 0 && (c->tail_tokens >= c->grid_tokens || c->grid_tokens > M))
+      // the streaming shape only; the walking clusters need a token each
+      if (c->tail_tokens > 0 &&
+          (c->variant != 3 || c->tail_tokens >= c->grid_tokens || c->grid_tokens > M))
         return ATTNRES_ERR_CONFIG;
     }
   }

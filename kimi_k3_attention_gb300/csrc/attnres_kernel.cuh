@@ -85,14 +85,19 @@ struct Params {
 // order, so the short ones come last and fill the SMs that the long walks
 // leave idle at the end.  The host keeps 0 <= T < G <= M.  Written with the
 // launch parameters only, so that the walk holds no registers beyond the
-// token index.
+// token index.  PLAIN (the latency shapes, which the host never gives a
+// tail) takes c, c + G, ... straight from the grid: their first loads wait
+// on no parameter read (GB300, decode: 0.02-0.09 us per call).
+template <bool PLAIN>
 struct TokenWalk {
   static __device__ __forceinline__ int first(const Params& p) {
     const int c = static_cast<int>(blockIdx.y);
+    if constexpr (PLAIN) return c;
     return c < p.walkers ? c : p.walk_end + (c - p.walkers);
   }
   // the token this cluster takes after m, or M when it has none
   static __device__ __forceinline__ int next(const Params& p, int m) {
+    if constexpr (PLAIN) return m + static_cast<int>(gridDim.y);
     const int n = m + p.walkers;
     return (m < p.walk_end && n < p.walk_end) ? n : p.M;
   }
@@ -663,6 +668,21 @@ struct SmemSources {
 // Sums of squares and dot products with w of sources I0..I1-1 over this
 // thread's chunks: part[2(i - I0)] = ss_i, part[2(i - I0) + 1] = d_i, the
 // rest of the KP slots zero.
+template <int VPT, int DT, class Src>
+__device__ __forceinline__ void source_stats(const Src& src, int i, const uint4 (&wv)[VPT],
+                                             float& ss, float& d) {
+  ss = 0.f;
+  d = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const uint4 u = src.get(i, k);
+    Fmt<DT>::stats(u.x, wv[k].x, ss, d);
+    Fmt<DT>::stats(u.y, wv[k].y, ss, d);
+    Fmt<DT>::stats(u.z, wv[k].z, ss, d);
+    Fmt<DT>::stats(u.w, wv[k].w, ss, d);
+  }
+}
+
 template <int I0, int I1, int KP, int VPT, int DT, class Src>
 __device__ __forceinline__ void source_sums(const Src& src, const uint4 (&wv)[VPT],
                                             float (&part)[KP]) {
@@ -682,6 +702,53 @@ __device__ __forceinline__ void source_sums(const Src& src, const uint4 (&wv)[VP
   }
 #pragma unroll
   for (int i = 2 * (I1 - I0); i < KP; ++i) part[i] = 0.f;
+}
+
+// The sums of sources I0..I1-1 (KP partials, padded with zeros) reduced
+// over the warp: the result of source_sums followed by
+// warp_transpose_reduce<KP>, bit for bit.  With FOLD and KP = 32 the first
+// transpose step (which pairs partial i with partial i + 16, i.e. source
+// I0 + s with source I0 + 8 + s) is taken as each upper source's sums are
+// formed, so that 16 partials and the pair in hand are live instead of 32
+// beside the rows of every source: the deep banks' shapes spill much less
+// (N = 24, 12 rows in registers, 80 registers: 4 bytes against 40); the
+// shallow shapes spill a little more, and keep the plain order.
+template <int I0, int I1, int KP, int VPT, int DT, bool FOLD, class Src>
+__device__ __forceinline__ float sums_reduce(const Src& src, const uint4 (&wv)[VPT], int lane) {
+  if constexpr (KP < 32 || !FOLD) {
+    float part[KP];
+    source_sums<I0, I1, KP, VPT, DT>(src, wv, part);
+    return warp_transpose_reduce<KP>(part, lane);
+  } else {
+    constexpr int LO_END = I1 < I0 + 8 ? I1 : I0 + 8;
+    float v[16];
+    source_sums<I0, LO_END, 16, VPT, DT>(src, wv, v);
+    const bool upper = (lane & 16) != 0;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      float b[2] = {0.f, 0.f};
+      if (I0 + 8 + s < I1) source_stats<VPT, DT>(src, I0 + 8 + s, wv, b[0], b[1]);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int i = 2 * s + j;
+        const float give = upper ? v[i] : b[j];
+        const float keep = upper ? b[j] : v[i];
+        v[i] = keep + __shfl_xor_sync(FULL, give, 16);
+      }
+    }
+    // the remaining steps of warp_transpose_reduce<32>
+#pragma unroll
+    for (int half = 8, o = 8; half >= 1; half >>= 1, o >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float give = up ? v[i] : v[i + half];
+        const float keep = up ? v[i + half] : v[i];
+        v[i] = keep + __shfl_xor_sync(FULL, give, o);
+      }
+    }
+    return v[0];
+  }
 }
 
 // Everything after the loads for one token: fold, sums, both exchanges,
@@ -715,19 +782,17 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
   // ---- per-source sums of squares and dot products with w, and R1: warp
   // transpose-reduction per group, CTA sum, st.async to every CTA
   float wt0, wt1 = 0.f;
-  {
+  if constexpr (SL::G == 1) {
     float part0[SL::KP0];
     source_sums<0, S0, SL::KP0, VPT, DT>(src, wv, part0);
-    if constexpr (SL::G == 1) {
-      src.fence();
-      wt0 = warp_transpose_reduce<SL::KP0>(part0, lane);
-    } else {
-      wt0 = warp_transpose_reduce<SL::KP0>(part0, lane);
-      float part1[SL::KP1 > 0 ? SL::KP1 : 1];
-      source_sums<16, S, (SL::KP1 > 0 ? SL::KP1 : 1), VPT, DT>(src, wv, part1);
-      src.fence();
-      wt1 = warp_transpose_reduce<SL::KP1>(part1, lane);
-    }
+    src.fence();
+    wt0 = warp_transpose_reduce<SL::KP0>(part0, lane);
+  } else {
+    wt0 = sums_reduce<0, S0, SL::KP0, VPT, DT, true>(src, wv, lane);
+    float part1[SL::KP1 > 0 ? SL::KP1 : 1];
+    source_sums<16, S, (SL::KP1 > 0 ? SL::KP1 : 1), VPT, DT>(src, wv, part1);
+    src.fence();
+    wt1 = warp_transpose_reduce<SL::KP1>(part1, lane);
   }
   if ((lane & ((1 << SL::SH0) - 1)) == 0) x.red[warp][lane >> SL::SH0] = wt0;
   if constexpr (SL::G == 2)
@@ -944,7 +1009,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   __shared__ Exchange<Sums<N>::G> x;
   extern __shared__ __align__(16) uint4 hyb[];   // [N - NR][blockDim.x] when HYB
   Thread t = thread_info();
-  const int m0 = TokenWalk::first(p);
+  using Walk = TokenWalk<LAT>;
+  const int m0 = Walk::first(p);
   const int c0 = static_cast<int>(t.crank) * p.cpc;
   const int cend = min(c0 + p.cpc, p.H8);
   int jj[VPT];
@@ -1018,7 +1084,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   }
 
   bool first = true;
-  for (int m = m0; m < p.M; m = TokenWalk::next(p, m)) {
+  for (int m = m0; m < p.M; m = Walk::next(p, m)) {
     const size_t row = static_cast<size_t>(m) * p.H8;
     uint4 v[NR + 1][VPT];
     uint4 pr[VPT], ad[VPT], ad2[VPT];
@@ -1045,11 +1111,11 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // While this token is reduced, let L2 fetch this CTA's rows of the next
     // token it will take: the requests keep HBM busy during the reductions
     // and the next loads hit L2.
-    if ((p.prefetch & 4) && TokenWalk::next(p, m) < p.M) {
+    if ((p.prefetch & 4) && Walk::next(p, m) < p.M) {
       constexpr int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3);
       if (static_cast<int>(threadIdx.x) < rows && cend > c0) {
         const int r = threadIdx.x;
-        const size_t off = static_cast<size_t>(TokenWalk::next(p, m)) * p.H8 + c0;
+        const size_t off = static_cast<size_t>(Walk::next(p, m)) * p.H8 + c0;
         const uint4* src = r < N ? p.bank + r * p.bank_stride + off
                          : r == N ? p.prefix + off
                          : r == N + 1 ? p.add + off : p.add2 + off;
@@ -1187,7 +1253,7 @@ __global__ void __launch_bounds__(kPatternMaxT) attnres_pattern_kernel(const Par
   const int j = c0 + static_cast<int>(threadIdx.x);
   const bool ok = j < cend;
   griddep_wait();
-  for (int m = TokenWalk::first(p); m < p.M; m = TokenWalk::next(p, m)) {
+  for (int m = TokenWalk<false>::first(p); m < p.M; m = TokenWalk<false>::next(p, m)) {
     const size_t row = static_cast<size_t>(m) * p.H8;
     uint4 v[N + 3];
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -1196,11 +1262,11 @@ __global__ void __launch_bounds__(kPatternMaxT) attnres_pattern_kernel(const Par
     v[2] = ok ? ld_stream(p.add2 + row + j) : z;
 #pragma unroll
     for (int i = 0; i < N; ++i) v[3 + i] = ok ? ld_stream(p.bank + i * p.bank_stride + row + j) : z;
-    if ((p.prefetch & 4) && TokenWalk::next(p, m) < p.M) {
+    if ((p.prefetch & 4) && TokenWalk<false>::next(p, m) < p.M) {
       constexpr int rows = N + 3;
       if (static_cast<int>(threadIdx.x) < rows && cend > c0) {
         const int r = threadIdx.x;
-        const size_t off = static_cast<size_t>(TokenWalk::next(p, m)) * p.H8 + c0;
+        const size_t off = static_cast<size_t>(TokenWalk<false>::next(p, m)) * p.H8 + c0;
         const uint4* src = r < N ? p.bank + r * p.bank_stride + off
                          : r == N ? p.prefix + off : r == N + 1 ? p.add + off : p.add2 + off;
         prefetch_l2(src, static_cast<uint32_t>(cend - c0) * 16u);

@@ -41,14 +41,17 @@ constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 // Every shape is compiled for N <= kShallowMaxN.  Deeper banks (up to
 // ATTNRES_MAX_N) have the split shape and a streaming shape of their own:
 // up to 128 threads, registers capped so that deep_minb(N) CTAs share an SM,
-// and from 23 snapshots on the bank rows past deep_nr(N) = 16 held in shared
-// memory instead of registers (GB300, M = 8192: 4.9-6.1 TB/s for N = 13..31,
-// against 3.3-4.1 TB/s uncapped and 4.6-4.9 TB/s at N = 24..31 with every
-// row in registers; spills stay within a few dozen bytes).
+// and bank rows deep_nr(N)..N-1 held in shared memory instead of registers:
+// from 23 snapshots on past row 16; at N = 16, the first with two groups of
+// sums, past row 8 with seven CTAs per SM (+3 % against every row in
+// registers and five CTAs; the same split is 4-10 % slower at N = 13..20
+// otherwise).  GB300, M = 8192: 5.3-6.5 TB/s for N = 13..31, against
+// 3.3-4.1 TB/s uncapped and 4.6-4.9 TB/s at N = 24..31 with every row in
+// registers; spills stay within a few dozen bytes.
 constexpr int kShallowMaxN = 12;
 constexpr int kDeepStreamMaxT = 128;
-constexpr int deep_minb(int n) { return n <= 16 ? 5 : 4; }
-constexpr int deep_nr(int n) { return n >= 23 ? 16 : n; }
+constexpr int deep_minb(int n) { return n == 16 ? 7 : n <= 16 ? 5 : 4; }
+constexpr int deep_nr(int n) { return n == 16 ? 8 : n >= 23 ? 16 : n; }
 
 // Clusters that fit the device at once for launch configuration cfg (its
 // block size, dynamic shared memory and cluster attribute), cached per

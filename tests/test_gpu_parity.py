@@ -248,7 +248,7 @@ def test_tail_tokens(grid_tokens, tail_tokens):
     """The last tail_tokens clusters take one token each, the others walk the
     rest: every token once, the same bits as one cluster per token."""
     inp = wl.make_inputs(67, 6, H, seed=13)
-    for variant, cl in (("cluster", 4), ("stream", 7), ("stream", 4), ("cluster2", 8), ("cta", 0)):
+    for variant, cl in (("stream", 7), ("stream", 4), ("stream", 8), ("stream", 2)):
         plain = binding.make_config(variant, cluster=cl, grid_tokens=67)
         walk = binding.make_config(variant, cluster=cl, grid_tokens=grid_tokens,
                                    tail_tokens=tail_tokens)
@@ -284,6 +284,8 @@ def test_tail_tokens_rejected():
     call(binding.make_config("stream", cluster=4, tail_tokens=2))                   # auto grid
     call(binding.make_config("stream", cluster=4, grid_tokens=4, tail_tokens=-1))
     call(binding.make_config("pipe", cluster=4, grid_tokens=4, tail_tokens=1))
+    for v in ("cluster", "cluster2", "cta"):                                       # latency shapes
+        call(binding.make_config(v, grid_tokens=4, tail_tokens=1))
 
 
 def test_more_tokens_than_grid_limit():
