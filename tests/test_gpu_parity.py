@@ -248,7 +248,7 @@ def test_tail_tokens(grid_tokens, tail_tokens):
     """The last tail_tokens clusters take one token each, the others walk the
     rest: every token once, the same bits as one cluster per token."""
     inp = wl.make_inputs(67, 6, H, seed=13)
-    for variant, cl in (("stream", 7), ("stream", 4), ("stream", 8), ("stream", 2)):
+    for variant, cl in (("stream", 7), ("stream", 4), ("stream", 8), ("stream", 5)):
         plain = binding.make_config(variant, cluster=cl, grid_tokens=67)
         walk = binding.make_config(variant, cluster=cl, grid_tokens=grid_tokens,
                                    tail_tokens=tail_tokens)
