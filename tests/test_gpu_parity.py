@@ -272,6 +272,22 @@ def test_automatic_walk(M, N):
     assert_parity(inp, gnp, gout, tokens=toks)
 
 
+@pytest.mark.parametrize("M,N,fp16", [(1500, 16, False), (900, 24, False), (700, 31, False),
+                                       (1200, 12, True), (600, 20, True)])
+def test_automatic_walk_deep_and_fp16(M, N, fp16):
+    """The launch-time walk of the deep streaming shapes and of FP16 tensors:
+    the same bits as one cluster per token, parity with the oracle."""
+    inp = wl.make_inputs(M, N, H, seed=16 + M + N, add2=True,
+                         dtype=torch.float16 if fp16 else torch.bfloat16)
+    plan = binding.attnres_plan(M, N, H)
+    assert plan["variant"] == 3 and plan["grid_tokens"] == 0
+    gnp, gout = run_gpu(inp)
+    rnp, rout = run_gpu(inp, binding.make_config("stream", cluster=plan["cluster"], grid_tokens=M))
+    assert (gnp == rnp).all() and (gout == rout).all()
+    toks = np.unique(np.linspace(0, M - 1, 40).astype(int))
+    assert_parity(inp, gnp, gout, tokens=toks)
+
+
 def test_tail_tokens_rejected():
     inp = wl.make_inputs(9, 2, H, seed=15).to("cuda")
     out, np_ = torch.empty_like(inp.prefix), torch.empty_like(inp.prefix)
