@@ -339,6 +339,18 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU legs
 
+def after_current(*streams):
+    """Order `streams` after the work already queued on the current stream.
+    The inputs are drawn there, and the caching allocator may hand a block
+    that a queued kernel of the current stream still reads (a float32
+    temporary of the draws) to an output buffer: a kernel on another stream
+    writing that buffer before the draws finish would corrupt the inputs."""
+    import torch
+    cur = torch.cuda.current_stream()
+    for st in streams:
+        st.wait_stream(cur)
+
+
 def time_bandwidth(binding, inp, steps, warmup, stream, config=None):
     """Set up K back-to-back calls, each to be bracketed by CUDA events on
     `stream`; runs the warm-up calls."""
@@ -348,6 +360,7 @@ def time_bandwidth(binding, inp, steps, warmup, stream, config=None):
     call = lambda: binding.attnres_add_rmsnorm(inp.prefix, inp.add, inp.add2, inp.bank, inp.w,  # noqa: E731
                                                inp.gamma, inp.eps, out, newp, stream=stream, check=False,
                                                config=config)
+    after_current(stream)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             call()
@@ -395,6 +408,7 @@ def _decode_shape_times(binding, M, N, configs, seed, reps=200, replays=20):
         return round(statistics.median(out), 3)
 
     res = {}
+    after_current(s)
     for name, cfg in configs.items():
         def call(i, cfg=cfg):
             binding.attnres_add_rmsnorm(P[i], A[i], A2[i], B[i], w, gam, 1e-6, O[i], NP[i],
@@ -464,6 +478,7 @@ def pattern_ceiling(binding, inp, nbytes, peak, steps=10, warmup=3):
 
     def call():
         binding.attnres_access_pattern(inp.prefix, inp.add, inp.add2, inp.bank, out, newp, stream=s)
+    after_current(s)
     with torch.cuda.stream(s):
         for _ in range(warmup):
             call()
@@ -488,6 +503,7 @@ def _graph_us(build_calls, s, replays=20):
     """Capture build_calls() (which enqueues `n` calls on stream s and returns
     n) in a CUDA graph; median microseconds per call over `replays`."""
     import torch
+    after_current(s)
     with torch.cuda.stream(s):
         build_calls()
     torch.cuda.synchronize()
@@ -570,6 +586,7 @@ def _domain_row(binding, wl, N, dtype, peak, seed, steps=5, warmup=3):
 
     def call():
         binding.attnres_add_rmsnorm(P, A, A2, B, w, gam, 1e-6, out, newp, stream=s, check=False)
+    after_current(s)
     with torch.cuda.stream(s):
         for _ in range(warmup):
             call()
@@ -672,6 +689,7 @@ def run_e2e(binding, inp, out, newp, stream, args, nbytes, barrier, max_ranks, w
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = 2 * out.numel() * out.element_size()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    after_current(up, stream, down)
     ev = lambda: torch.cuda.Event()  # noqa: E731
     uploaded = [ev(), ev()]
     computed = [ev(), ev()]

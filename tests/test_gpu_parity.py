@@ -632,6 +632,7 @@ def test_cuda_graph_capture_and_replay():
     d = inp.to("cuda")
     s = torch.cuda.Stream()
     out, newp = torch.empty_like(d.prefix), torch.empty_like(d.prefix)
+    s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         binding.attnres_add_rmsnorm(d.prefix, d.add, d.add2, d.bank, d.w, d.gamma, d.eps, out, newp,
                                     stream=s)
