@@ -85,9 +85,10 @@ cudaError_t resident_clusters(Kern kern, cudaLaunchConfig_t cfg, int dev, int cl
 // started last, fill the slots that finish early.  Every cluster costs a
 // start (its first token is not prefetched): L minimises the clusters per
 // slot, M / (L R) + L / 2.  GB300, N = 12, against 10 clusters per SM each
-// walking an equal share: +2 % at M = 8192 and 16384, +5 % at M = 4096,
-// every cell of a sweep of (M - T) / L and T around this choice within 1 %
-// of the best.  L < 2: one cluster per token.
+// walking an equal share (one cluster per token below 1520 tokens): +2 % at
+// M = 8192 and 16384, +5 % at 4096, +7..11 % at 256..2048; every cell of a
+// sweep of (M - T) / L and T around this choice within 1 % of the best.
+// L < 2: one cluster per token.
 inline void walk_grid(int M, int R, unsigned* gy, int* tail) {
   const long long L = std::llround(std::sqrt(2.0 * M / (R > 0 ? R : 1)));
   if (L < 2) {
