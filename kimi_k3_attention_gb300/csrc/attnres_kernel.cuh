@@ -90,14 +90,15 @@ struct Params {
 // on no parameter read (GB300, decode: 0.02-0.09 us per call).
 template <bool PLAIN>
 struct TokenWalk {
-  static __device__ __forceinline__ int first(const Params& p) {
-    const int c = static_cast<int>(blockIdx.y);
+  // the first token of cluster c (blockIdx.y)
+  static __host__ __device__ __forceinline__ int first(const Params& p, int c) {
     if constexpr (PLAIN) return c;
     return c < p.walkers ? c : p.walk_end + (c - p.walkers);
   }
-  // the token this cluster takes after m, or M when it has none
-  static __device__ __forceinline__ int next(const Params& p, int m) {
-    if constexpr (PLAIN) return m + static_cast<int>(gridDim.y);
+  // the token a cluster takes after m in a grid of G clusters (gridDim.y),
+  // or M when it has none
+  static __host__ __device__ __forceinline__ int next(const Params& p, int m, int G) {
+    if constexpr (PLAIN) return m + G;
     const int n = m + p.walkers;
     return (m < p.walk_end && n < p.walk_end) ? n : p.M;
   }
@@ -1010,7 +1011,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   extern __shared__ __align__(16) uint4 hyb[];   // [N - NR][blockDim.x] when HYB
   Thread t = thread_info();
   using Walk = TokenWalk<LAT>;
-  const int m0 = Walk::first(p);
+  const int m0 = Walk::first(p, static_cast<int>(blockIdx.y));
   const int c0 = static_cast<int>(t.crank) * p.cpc;
   const int cend = min(c0 + p.cpc, p.H8);
   int jj[VPT];
@@ -1084,7 +1085,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   }
 
   bool first = true;
-  for (int m = m0; m < p.M; m = Walk::next(p, m)) {
+  for (int m = m0; m < p.M; m = Walk::next(p, m, static_cast<int>(gridDim.y))) {
     const size_t row = static_cast<size_t>(m) * p.H8;
     uint4 v[NR + 1][VPT];
     uint4 pr[VPT], ad[VPT], ad2[VPT];
@@ -1111,11 +1112,11 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // While this token is reduced, let L2 fetch this CTA's rows of the next
     // token it will take: the requests keep HBM busy during the reductions
     // and the next loads hit L2.
-    if ((p.prefetch & 4) && Walk::next(p, m) < p.M) {
+    if ((p.prefetch & 4) && Walk::next(p, m, static_cast<int>(gridDim.y)) < p.M) {
       constexpr int rows = N + (MODE == kNoFold ? 1 : MODE == kFoldAdd ? 2 : 3);
       if (static_cast<int>(threadIdx.x) < rows && cend > c0) {
         const int r = threadIdx.x;
-        const size_t off = static_cast<size_t>(Walk::next(p, m)) * p.H8 + c0;
+        const size_t off = static_cast<size_t>(Walk::next(p, m, static_cast<int>(gridDim.y))) * p.H8 + c0;
         const uint4* src = r < N ? p.bank + r * p.bank_stride + off
                          : r == N ? p.prefix + off
                          : r == N + 1 ? p.add + off : p.add2 + off;
@@ -1253,7 +1254,9 @@ __global__ void __launch_bounds__(kPatternMaxT) attnres_pattern_kernel(const Par
   const int j = c0 + static_cast<int>(threadIdx.x);
   const bool ok = j < cend;
   griddep_wait();
-  for (int m = TokenWalk<false>::first(p); m < p.M; m = TokenWalk<false>::next(p, m)) {
+  const int G = static_cast<int>(gridDim.y);
+  for (int m = TokenWalk<false>::first(p, static_cast<int>(blockIdx.y)); m < p.M;
+       m = TokenWalk<false>::next(p, m, G)) {
     const size_t row = static_cast<size_t>(m) * p.H8;
     uint4 v[N + 3];
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -1262,11 +1265,11 @@ __global__ void __launch_bounds__(kPatternMaxT) attnres_pattern_kernel(const Par
     v[2] = ok ? ld_stream(p.add2 + row + j) : z;
 #pragma unroll
     for (int i = 0; i < N; ++i) v[3 + i] = ok ? ld_stream(p.bank + i * p.bank_stride + row + j) : z;
-    if ((p.prefetch & 4) && TokenWalk<false>::next(p, m) < p.M) {
+    if ((p.prefetch & 4) && TokenWalk<false>::next(p, m, G) < p.M) {
       constexpr int rows = N + 3;
       if (static_cast<int>(threadIdx.x) < rows && cend > c0) {
         const int r = threadIdx.x;
-        const size_t off = static_cast<size_t>(TokenWalk<false>::next(p, m)) * p.H8 + c0;
+        const size_t off = static_cast<size_t>(TokenWalk<false>::next(p, m, G)) * p.H8 + c0;
         const uint4* src = r < N ? p.bank + r * p.bank_stride + off
                          : r == N ? p.prefix + off : r == N + 1 ? p.add + off : p.add2 + off;
         prefetch_l2(src, static_cast<uint32_t>(cend - c0) * 16u);
