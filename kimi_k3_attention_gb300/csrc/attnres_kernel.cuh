@@ -104,6 +104,10 @@ struct TokenWalk {
   }
 };
 
+// Every shape is compiled for up to kShallowMaxN snapshots; deeper banks
+// (up to 31) have shapes of their own (attnres_launch.cuh).
+constexpr int kShallowMaxN = 12;
+
 // What a launch does with the prefix sum.
 //   kFoldAdd:  new_prefix = bf16(prefix + add)            (no second addend)
 //   kFoldAdd2: new_prefix = bf16(prefix + bf16(add + add2))
@@ -552,6 +556,7 @@ struct alignas(16) Exchange {
   float red[16][32 * G];   // up to 16 warps (448-thread CTAs have 14)
   float xin1[16][32 * G];  // up to 16 CTAs per cluster
   float xin2[256];         // 16 CTAs x 16 warps
+  float alpha[32 * G];     // softmax weights (shapes where one warp evaluates it)
   unsigned long long bar1;
   unsigned long long bar2;
 };
@@ -758,7 +763,7 @@ __device__ __forceinline__ float sums_reduce(const Src& src, const uint4 (&wv)[V
 // wv the pseudo-query chunks; masked chunks (ok false) are zeros and store
 // nothing.  LAT (the latency shapes) adds the R2 partials in every lane
 // instead of with shuffles: the same bits, a shorter dependent chain.
-template <int N, int MODE, int VPT, int DT, bool LAT, class Src>
+template <int N, int MODE, int VPT, int DT, bool LAT, bool SMX, class Src>
 __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>::G>& x, Thread& t,
                                                size_t row, const int (&jj)[VPT],
                                                const bool (&ok)[VPT], const uint4 (&wv)[VPT],
@@ -822,40 +827,65 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
   }
   exchange_wait(bar1, t, p);
   if (threadIdx.x == 0 && !t.failed) mbar_arm(bar1, r1_bytes(SL::total, t, p));  // next token
-  // cluster totals: lane l of tot[g] holds sum 32 g + l
-  float tot[SL::G];
+  // ---- cluster totals, logits and softmax (in one warp: lane i < S returns
+  // the weight of source i)
+  auto softmax = [&]() -> float {
+    // cluster totals: lane l of tot[g] holds sum 32 g + l
+    float tot[SL::G];
 #pragma unroll
-  for (int g = 0; g < SL::G; ++g) {
-    const int kp = g == 0 ? SL::KP0 : SL::KP1;
-    tot[g] = 0.f;
-    if (lane < kp) {
+    for (int g = 0; g < SL::G; ++g) {
+      const int kp = g == 0 ? SL::KP0 : SL::KP1;
+      tot[g] = 0.f;
+      if (lane < kp) {
 #pragma unroll
-      for (uint32_t c = 0; c < 16; ++c)
-        if (c < t.csize) tot[g] += x.xin1[c][32 * g + lane];
+        for (uint32_t c = 0; c < 16; ++c)
+          if (c < t.csize) tot[g] += x.xin1[c][32 * g + lane];
+      }
     }
-  }
 
-  // ---- logits and softmax, lane i < S holds source i (sums 2i and 2i + 1
-  // sit in group i / 16 at lanes (2i) mod 32 and (2i + 1) mod 32)
-  float ss_i = __shfl_sync(FULL, tot[0], (2 * lane) & 31);
-  float d_i = __shfl_sync(FULL, tot[0], (2 * lane + 1) & 31);
-  if constexpr (SL::G == 2) {
-    const float ss1 = __shfl_sync(FULL, tot[SL::G - 1], (2 * lane) & 31);
-    const float d1 = __shfl_sync(FULL, tot[SL::G - 1], (2 * lane + 1) & 31);
-    if (lane >= 16) {
-      ss_i = ss1;
-      d_i = d1;
+    // logits and softmax, lane i < S holds source i (sums 2i and 2i + 1 sit
+    // in group i / 16 at lanes (2i) mod 32 and (2i + 1) mod 32)
+    float ss_i = __shfl_sync(FULL, tot[0], (2 * lane) & 31);
+    float d_i = __shfl_sync(FULL, tot[0], (2 * lane + 1) & 31);
+    if constexpr (SL::G == 2) {
+      const float ss1 = __shfl_sync(FULL, tot[SL::G - 1], (2 * lane) & 31);
+      const float d1 = __shfl_sync(FULL, tot[SL::G - 1], (2 * lane + 1) & 31);
+      if (lane >= 16) {
+        ss_i = ss1;
+        d_i = d1;
+      }
     }
-  }
-  const float logit = (lane < S) ? rsqrtf(__fmaf_rn(ss_i, p.inv_h, p.eps)) * d_i : -INFINITY;
-  // up to 16 sources sit in lanes 0..15: reduce over 16 lanes, else 32
-  const float mx = S <= 16 ? half_warp_max(logit) : warp_max(logit);
-  const float ex = (lane < S) ? __expf(logit - mx) : 0.f;
-  const float den = S <= 16 ? half_warp_sum(ex) : warp_sum(ex);
-  const float alpha_l = ex / den;
+    const float logit = (lane < S) ? rsqrtf(__fmaf_rn(ss_i, p.inv_h, p.eps)) * d_i : -INFINITY;
+    // up to 16 sources sit in lanes 0..15: reduce over 16 lanes, else 32
+    const float mx = S <= 16 ? half_warp_max(logit) : warp_max(logit);
+    const float ex = (lane < S) ? __expf(logit - mx) : 0.f;
+    const float den = S <= 16 ? half_warp_sum(ex) : warp_sum(ex);
+    return ex / den;
+  };
   float alpha[S];
+  if constexpr (SMX) {
+    // the streaming shapes of up to 12 snapshots: one warp evaluates the
+    // softmax, the others read the weights after a CTA barrier (its next
+    // write follows the next token's R1 barrier, which every warp passes
+    // after these reads).  GB300, same-box A/B: M = 8192 +1..3 % at
+    // N = 1..9 and FP16 N = 12, BF16 N = 12 unchanged, M = 96 +4 %; with the
+    // four to seven CTAs per SM of the deep shapes the barrier cost 14-19 %,
+    // so those keep every warp evaluating it (as do the latency shapes,
+    // where it would add a barrier to the critical path).
+    if (warp == 0) {
+      const float alpha_l = softmax();
+      if (lane < S) x.alpha[lane] = alpha_l;
+    }
+    __syncthreads();
 #pragma unroll
-  for (int i = 0; i < S; ++i) alpha[i] = __shfl_sync(FULL, alpha_l, i);
+    for (int i = 0; i < S; ++i) alpha[i] = x.alpha[i];
+  } else {
+    // every warp evaluates it from identical totals in identical order:
+    // bit-identical weights everywhere, no barrier
+    const float alpha_l = softmax();
+#pragma unroll
+    for (int i = 0; i < S; ++i) alpha[i] = __shfl_sync(FULL, alpha_l, i);
+  }
 
   // ---- mixture h = sum_i alpha_i v_i, and sum h^2
   float h[VPT][8];
@@ -1007,6 +1037,8 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // the latency shapes (split, split with two CTAs per SM, one CTA per
   // token): at most a few warps per SM, latency rather than issue bound
   constexpr bool LAT = (MINB <= 2) && (MAXT >= 256);
+  // one warp evaluates the softmax: the streaming shapes of up to 12 snapshots
+  constexpr bool SMX = !LAT && N <= kShallowMaxN;
   __shared__ Exchange<Sums<N>::G> x;
   extern __shared__ __align__(16) uint4 hyb[];   // [N - NR][blockDim.x] when HYB
   Thread t = thread_info();
@@ -1130,10 +1162,10 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     if constexpr (HYB) {
       cp_async_wait<0>();   // this thread's own slots: no barrier needed
       HybridSources<N, NR> src{v, hyb0, hstep, ok[0]};
-      token_epilogue<N, MODE, VPT, DT, LAT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
+      token_epilogue<N, MODE, VPT, DT, LAT, SMX>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
     } else {
       RegSources<N, VPT> src{v};
-      token_epilogue<N, MODE, VPT, DT, LAT>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
+      token_epilogue<N, MODE, VPT, DT, LAT, SMX>(p, x, t, row, jj, ok, wv, gv, pr, ad, ad2, src, first);
     }
   }
   exchange_exit(t, p);
@@ -1210,7 +1242,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
       a += row_step;
     }
     SmemSources<N> src{a, row_step, ok[0], z};
-    token_epilogue<N, ADD2 ? kFoldAdd2 : kFoldAdd, 1, kBF16, false>(p, x, t, static_cast<size_t>(m) * p.H8, jj,
+    token_epilogue<N, ADD2 ? kFoldAdd2 : kFoldAdd, 1, kBF16, false, false>(p, x, t, static_cast<size_t>(m) * p.H8, jj,
                                                      ok, wv, gv, pr, ad, ad2, src, first);
     stage = (stage + 1 == STAGES) ? 0 : stage + 1;
   }

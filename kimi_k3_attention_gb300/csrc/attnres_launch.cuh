@@ -48,7 +48,6 @@ constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 // otherwise).  GB300, M = 8192: 5.3-6.5 TB/s for N = 13..31, against
 // 3.3-4.1 TB/s uncapped and 4.6-4.9 TB/s at N = 24..31 with every row in
 // registers; spills stay within a few dozen bytes.
-constexpr int kShallowMaxN = 12;
 constexpr int kDeepStreamMaxT = 128;
 constexpr int deep_minb(int n) { return n == 16 ? 7 : n <= 16 ? 5 : 4; }
 constexpr int deep_nr(int n) { return n == 16 ? 8 : n >= 23 ? 16 : n; }
