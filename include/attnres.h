@@ -46,12 +46,14 @@
  *     is asynchronous).  The one the kernels detect is a CTA of a cluster
  *     waiting longer than a time limit (200 ms) for its peers' partial
  *     sums, which happens only if the GPU does not run the CTAs of a cluster
- *     together.  The kernel then finishes without hanging, writes NaN into
- *     every element of out (and h_out) that depended on the exchange
- *     (new_prefix does not, and stays exact), and sets a bit that
- *     attnres_device_status() reports.  A caller that must not consume such
- *     outputs checks that status word after synchronising, or tests out for
- *     NaN.
+ *     together.  The kernel then finishes without hanging: the CTAs that
+ *     gave up write NaN into their part of out (and h_out), new_prefix
+ *     (which does not depend on the exchange) stays exact, and a bit is set
+ *     that attnres_device_status() reports.  A caller that must not consume
+ *     such outputs checks that status word after synchronising; when it is
+ *     set, no out or h_out value of that call is to be trusted (a CTA that
+ *     was itself the late one may finish on sums of several tokens without
+ *     writing NaN).
  *   - Aliasing: new_prefix may be exactly prefix (in-place carry-on of the
  *     prefix sum) or any region that overlaps no input (e.g. bank slot N,
  *     which the call does not read).  out may overlap nothing.
