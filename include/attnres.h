@@ -145,8 +145,8 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *             Variants 1, 4 and 5 exist for N <= 12 only (variant 5 with
  *             the fold on BF16 tensors only).  For N > 12
  *             variant 3 takes at most 128 threads, registers capped so
- *             that four to seven CTAs share an SM (at N = 16 with bank
- *             rows 8..15, from N = 23 on with rows 16..N-1, in dynamic
+ *             that four or five CTAs share an SM (at N = 15..17 with bank
+ *             rows 14..N-1, from N = 23 on with rows 16..N-1, in dynamic
  *             shared memory).
  *             4 = persistent and pipelined (the large-M streaming kernel): a
  *                 grid of as many clusters as fit the GPU at once walks the

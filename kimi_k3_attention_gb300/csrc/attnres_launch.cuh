@@ -41,16 +41,18 @@ constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 // Every shape is compiled for N <= kShallowMaxN.  Deeper banks (up to
 // ATTNRES_MAX_N) have the split shape and a streaming shape of their own:
 // up to 128 threads, registers capped so that deep_minb(N) CTAs share an SM,
-// and bank rows deep_nr(N)..N-1 held in shared memory instead of registers:
-// from 23 snapshots on past row 16; at N = 16, the first with two groups of
-// sums, past row 8 with seven CTAs per SM (+3 % against every row in
-// registers and five CTAs; the same split is 4-10 % slower at N = 13..20
-// otherwise).  GB300, M = 8192: 5.3-6.5 TB/s for N = 13..31, against
-// 3.3-4.1 TB/s uncapped and 4.6-4.9 TB/s at N = 24..31 with every row in
-// registers; spills stay within a few dozen bytes.
+// and bank rows deep_nr(N)..N-1 held in shared memory instead of registers.
+// GB300, M = 8192, swept per N over the cap (4-8 CTAs per SM) and the rows
+// kept in registers (4..N): up to 14 snapshots every row in registers at
+// 96 registers (5 CTAs); 15..17 snapshots rows 14.. in shared memory at 96
+// registers (N = 16: 5.75 TB/s against 5.28 with every row in registers and
+// 5.45 with rows 8.. and 7 CTAs; N = 17: 5.77 against 5.54); 18..22 every row
+// in registers at 128 registers (4 CTAs; 96 registers spill 20-36 bytes and
+// lose 3-7 %); from 23 on rows 16.. in shared memory at 128 registers.
+// 4.9-6.5 TB/s over N = 13..31, against 3.3-4.1 TB/s uncapped.
 constexpr int kDeepStreamMaxT = 128;
-constexpr int deep_minb(int n) { return n == 16 ? 7 : n <= 16 ? 5 : 4; }
-constexpr int deep_nr(int n) { return n == 16 ? 8 : n >= 23 ? 16 : n; }
+constexpr int deep_minb(int n) { return n <= 17 ? 5 : 4; }
+constexpr int deep_nr(int n) { return (n >= 15 && n <= 17) ? 14 : n >= 23 ? 16 : n; }
 
 // Clusters that fit the device at once for launch configuration cfg (its
 // block size, dynamic shared memory and cluster attribute), cached per
