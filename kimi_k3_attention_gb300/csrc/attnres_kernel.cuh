@@ -7,8 +7,8 @@
 //
 //   load    prefix, add, add2, bank[0..N-1] chunks: 16-byte vector loads
 //           straight to registers (attnres_fused_kernel; a cluster may walk
-//           several tokens and ask L2 for the next one's rows while it
-//           reduces the current one), or cp.async copies into a per-thread
+//           several tokens (TokenWalk) and ask L2 for the next one's rows
+//           while it reduces the current one), or cp.async copies into a per-thread
 //           shared-memory ring several tokens ahead (attnres_pipe_kernel,
 //           persistent)
 //   fold    new_prefix = bf16(prefix + bf16(add + add2)), each addition
@@ -24,8 +24,11 @@
 //           memory, then every CTA stores its totals into the shared memory
 //           of every CTA of the cluster with st.async, each store counted on
 //           the receiver's mbarrier, which the receiver waits on
-//   softmax every warp evaluates logits and softmax redundantly from the same
-//           totals in the same order, so all warps of all CTAs agree bitwise
+//   softmax logits and softmax from the cluster totals in a fixed order:
+//           evaluated by every warp redundantly (latency and deep shapes: all
+//           warps of all CTAs agree bitwise, no barrier), or by one warp and
+//           read by the others after a CTA barrier (the streaming shapes of
+//           up to 12 snapshots)
 //   mix     h = sum_i alpha_i v_i from registers (no second read)
 //   R2      sum h^2: warp reduction, st.async to every CTA, mbarrier wait
 //   out     bf16(h * rsqrt(mean(h^2) + eps) * gamma) (FP16 for FP16 tensors)
