@@ -303,10 +303,10 @@ cudaError_t dispatch(int N, bool add2, const Params& p, dim3 g, int t, int c, bo
                      cudaStream_t s) {
 #define ATTNRES_CASE(n)                                                                  \
   case n:                                                                                \
-    return add2 ? launch_fused<n, kFoldAdd2, VPT, MAXT, minb_of(MINB, n, kFoldAdd2)>(      \
-                      p, g, t, c, pdl, s)                                                 \
-                : launch_fused<n, kFoldAdd, VPT, MAXT, minb_of(MINB, n, kFoldAdd)>(        \
-                      p, g, t, c, pdl, s);
+    return add2 ? launch_fused<n, kFoldAdd2, VPT, MAXT, minb_of(MINB, n, kFoldAdd2), kBF16, \
+                               nr_of(MINB, n, kFoldAdd2)>(p, g, t, c, pdl, s)              \
+                : launch_fused<n, kFoldAdd, VPT, MAXT, minb_of(MINB, n, kFoldAdd), kBF16,   \
+                               nr_of(MINB, n, kFoldAdd)>(p, g, t, c, pdl, s);
   switch (N) {
     ATTNRES_CASE(0)
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
@@ -323,7 +323,8 @@ cudaError_t dispatch_nofold(int N, const Params& p, dim3 g, int t, int c, bool p
                             cudaStream_t s) {
 #define ATTNRES_CASE(n) \
   case n:               \
-    return launch_fused<n, kNoFold, VPT, MAXT, minb_of(MINB, n, kNoFold)>(p, g, t, c, pdl, s);
+    return launch_fused<n, kNoFold, VPT, MAXT, minb_of(MINB, n, kNoFold), kBF16,          \
+                        nr_of(MINB, n, kNoFold)>(p, g, t, c, pdl, s);
   switch (N) {
     ATTNRES_CASE(0)
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)
@@ -353,12 +354,13 @@ cudaError_t dispatch_fp16(int N, int mode, const Params& p, dim3 g, int t, int c
 #define ATTNRES_CASE(n)                                                                    \
   case n:                                                                                  \
     return mode == kFoldAdd2                                                               \
-               ? launch_fused<n, kFoldAdd2, VPT, MAXT, minb_of(MINB, n, kFoldAdd2), kFP16>(   \
-                     p, g, t, c, pdl, s)                                                   \
+               ? launch_fused<n, kFoldAdd2, VPT, MAXT, minb_of(MINB, n, kFoldAdd2), kFP16,    \
+                              nr_of(MINB, n, kFoldAdd2)>(p, g, t, c, pdl, s)               \
            : mode == kFoldAdd                                                              \
-               ? launch_fused<n, kFoldAdd, VPT, MAXT, minb_of(MINB, n, kFoldAdd), kFP16>(     \
-                     p, g, t, c, pdl, s)                                                   \
-               : launch_fused<n, kNoFold, VPT, MAXT, minb_of(MINB, n, kNoFold), kFP16>(p, g, t, c, pdl, s);
+               ? launch_fused<n, kFoldAdd, VPT, MAXT, minb_of(MINB, n, kFoldAdd), kFP16,      \
+                              nr_of(MINB, n, kFoldAdd)>(p, g, t, c, pdl, s)                \
+               : launch_fused<n, kNoFold, VPT, MAXT, minb_of(MINB, n, kNoFold), kFP16,        \
+                              nr_of(MINB, n, kNoFold)>(p, g, t, c, pdl, s);
   switch (N) {
     ATTNRES_CASE(0)
     ATTNRES_CASE(1) ATTNRES_CASE(2) ATTNRES_CASE(3) ATTNRES_CASE(4)

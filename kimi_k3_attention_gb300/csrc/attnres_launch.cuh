@@ -23,19 +23,30 @@ constexpr int kSplitVPT = 1, kSplitMaxT = 256, kSplitMinB = 1;
 // call runs, under programmatic dependent launch)
 constexpr int kSplit2MinB = 2;
 constexpr int kStreamVPT = 1, kStreamMaxT = 224;
-// The streaming shape's registers: capped at 72 (four CTAs of 224 threads,
-// or seven of 128, per SM) while a token has at most 12 rows (bank, prefix
-// and addends: N <= 9 with add2), which then fit without spilling, else at
-// 80 (three of 224, six of 128).  GB300, M = 8192, add2, the cap of 72
-// against 80: N = 2, 5..9 +2..8 %, N = 1, 3, 4 within 1 %; N = 10..12
-// (12-42 spilled bytes) -1..-9 %.
+// The streaming shape's registers and where a token's rows live.  With R
+// rows per token (bank, prefix and addends: stream_rows), registers are
+// capped at 56 (five CTAs of 224 threads, nine of 128, per SM) up to 6 rows
+// and at 72 (four of 224, seven of 128) beyond, and up to 11 rows stay in
+// registers, 11 of 12-13 and 12 of 14-15: the bank rows past that are
+// copied into the thread's own slots of shared memory (HybridSources), which
+// keeps the register allocation free of spills.  GB300, M = 8192, add2,
+// against every row in registers at 72 registers (80 from 13 rows on): N = 1
+// +5 %, N = 3 +4 %, N = 9 +1 %, N = 10 +3 %, N = 11 +1 %, N = 12 +2 %
+// (6.71-6.73 TB/s, about the copy peak); 56 registers beyond 6 rows and
+// fewer rows in registers spilled or lost 1-35 %.
 constexpr int stream_rows(int n, int mode) {
   return n + (mode == kFoldAdd2 ? 3 : mode == kFoldAdd ? 2 : 1);
 }
-constexpr int stream_minb(int n, int mode) { return stream_rows(n, mode) <= 12 ? 4 : 3; }
-// Dispatch's MINB for the streaming shape: stream_minb of each (N, mode).
+constexpr int stream_reg_rows(int r) { return r <= 11 ? r : r <= 13 ? 11 : 12; }
+constexpr int stream_minb(int n, int mode) { return stream_rows(n, mode) <= 6 ? 5 : 4; }
+constexpr int stream_nr(int n, int mode) {
+  return n - (stream_rows(n, mode) - stream_reg_rows(stream_rows(n, mode)));
+}
+// Dispatch's MINB for the streaming shape: stream_minb and stream_nr of each
+// (N, mode); the other shapes keep every row in registers.
 constexpr int kStreamMinB = 0;
 constexpr int minb_of(int minb, int n, int mode) { return minb != 0 ? minb : stream_minb(n, mode); }
+constexpr int nr_of(int minb, int n, int mode) { return minb != 0 ? n : stream_nr(n, mode); }
 constexpr int kCtaVPT = 2, kCtaMaxT = 448, kCtaMinB = 1;
 
 // Every shape is compiled for N <= kShallowMaxN.  Deeper banks (up to
@@ -323,8 +334,9 @@ cudaError_t launch_pattern(const Params& p, dim3 grid, int threads, int cluster,
 #define ATTNRES_INSTANTIATE(DEF, N, ADD2)                                                   \
   ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB)     \
   ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kSplitVPT, kSplitMaxT, kSplit2MinB)    \
-  ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kStreamVPT, kStreamMaxT,              \
-                stream_minb(N, ADD2 ? kFoldAdd2 : kFoldAdd))                                \
+  ATTNRES_FUSED_NR(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kStreamVPT, kStreamMaxT,           \
+                   stream_minb(N, ADD2 ? kFoldAdd2 : kFoldAdd), kBF16,                      \
+                   stream_nr(N, ADD2 ? kFoldAdd2 : kFoldAdd))                               \
   ATTNRES_FUSED(DEF, N, ADD2 ? kFoldAdd2 : kFoldAdd, kCtaVPT, kCtaMaxT, kCtaMinB)           \
   ATTNRES_PIPE(DEF, N, ADD2, 2)                                                             \
   ATTNRES_PIPE(DEF, N, ADD2, 3)                                                             \
@@ -334,7 +346,8 @@ cudaError_t launch_pattern(const Params& p, dim3 grid, int threads, int cluster,
 // streaming shapes.
 #define ATTNRES_INSTANTIATE_NOFOLD(DEF, N)                               \
   ATTNRES_FUSED(DEF, N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB)      \
-  ATTNRES_FUSED(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, stream_minb(N, kNoFold))
+  ATTNRES_FUSED_NR(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, stream_minb(N, kNoFold), kBF16, \
+                   stream_nr(N, kNoFold))
 
 // Deep banks, 13 <= N <= 31: the split shape and the deep streaming shape,
 // with the fold (add2 present or not) and without, for element format DT.
@@ -354,9 +367,12 @@ cudaError_t launch_pattern(const Params& p, dim3 grid, int threads, int cluster,
   ATTNRES_FUSED_DT(DEF, N, kFoldAdd2, kSplitVPT, kSplitMaxT, kSplitMinB, kFP16)        \
   ATTNRES_FUSED_DT(DEF, N, kFoldAdd, kSplitVPT, kSplitMaxT, kSplitMinB, kFP16)         \
   ATTNRES_FUSED_DT(DEF, N, kNoFold, kSplitVPT, kSplitMaxT, kSplitMinB, kFP16)          \
-  ATTNRES_FUSED_DT(DEF, N, kFoldAdd2, kStreamVPT, kStreamMaxT, stream_minb(N, kFoldAdd2), kFP16) \
-  ATTNRES_FUSED_DT(DEF, N, kFoldAdd, kStreamVPT, kStreamMaxT, stream_minb(N, kFoldAdd), kFP16)   \
-  ATTNRES_FUSED_DT(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, stream_minb(N, kNoFold), kFP16)
+  ATTNRES_FUSED_NR(DEF, N, kFoldAdd2, kStreamVPT, kStreamMaxT, stream_minb(N, kFoldAdd2), kFP16, \
+                   stream_nr(N, kFoldAdd2))                                                  \
+  ATTNRES_FUSED_NR(DEF, N, kFoldAdd, kStreamVPT, kStreamMaxT, stream_minb(N, kFoldAdd), kFP16,   \
+                   stream_nr(N, kFoldAdd))                                                   \
+  ATTNRES_FUSED_NR(DEF, N, kNoFold, kStreamVPT, kStreamMaxT, stream_minb(N, kNoFold), kFP16,     \
+                   stream_nr(N, kNoFold))
 
 #define ATTNRES_TAIL_ADD(DEF, ADD2, DT)                                                      \
   DEF template cudaError_t launch_tail_add<ADD2, DT>(const uint4*, const uint4*, const uint4*,  \
