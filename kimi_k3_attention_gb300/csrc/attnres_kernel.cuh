@@ -713,51 +713,45 @@ __device__ __forceinline__ void source_sums(const Src& src, const uint4 (&wv)[VP
   for (int i = 2 * (I1 - I0); i < KP; ++i) part[i] = 0.f;
 }
 
-// The sums of sources I0..I1-1 (KP partials, padded with zeros) reduced
-// over the warp: the result of source_sums followed by
-// warp_transpose_reduce<KP>, bit for bit.  With FOLD and KP = 32 the first
-// transpose step (which pairs partial i with partial i + 16, i.e. source
-// I0 + s with source I0 + 8 + s) is taken as each upper source's sums are
-// formed, so that 16 partials and the pair in hand are live instead of 32
-// beside the rows of every source: the deep banks' shapes spill much less
-// (N = 24, 12 rows in registers, 80 registers: 4 bytes against 40); the
-// shallow shapes spill a little more, and keep the plain order.
-template <int I0, int I1, int KP, int VPT, int DT, bool FOLD, class Src>
-__device__ __forceinline__ float sums_reduce(const Src& src, const uint4 (&wv)[VPT], int lane) {
-  if constexpr (KP < 32 || !FOLD) {
-    float part[KP];
-    source_sums<I0, I1, KP, VPT, DT>(src, wv, part);
-    return warp_transpose_reduce<KP>(part, lane);
-  } else {
-    constexpr int LO_END = I1 < I0 + 8 ? I1 : I0 + 8;
-    float v[16];
-    source_sums<I0, LO_END, 16, VPT, DT>(src, wv, v);
-    const bool upper = (lane & 16) != 0;
+// The sums of sources I0..I1-1 (32 partials, padded with zeros) reduced over
+// the warp: the result of source_sums followed by warp_transpose_reduce<32>,
+// bit for bit, with the first transpose step (which pairs partial i with
+// partial i + 16, i.e. source I0 + s with source I0 + 8 + s) taken as each
+// upper source's sums are formed, so that 16 partials and the pair in hand
+// are live instead of 32 beside the rows of every source.  The first group
+// of the deep banks' sums uses it: their shapes spill much less (N = 24, 12
+// rows in registers, 96 registers: 4 bytes against 40); the shallow shapes
+// spill a little more with it, and keep the plain order.
+template <int I0, int I1, int VPT, int DT, class Src>
+__device__ __forceinline__ float sums_reduce_folded(const Src& src, const uint4 (&wv)[VPT], int lane) {
+  constexpr int LO_END = I1 < I0 + 8 ? I1 : I0 + 8;
+  float v[16];
+  source_sums<I0, LO_END, 16, VPT, DT>(src, wv, v);
+  const bool upper = (lane & 16) != 0;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      float b[2] = {0.f, 0.f};
-      if (I0 + 8 + s < I1) source_stats<VPT, DT>(src, I0 + 8 + s, wv, b[0], b[1]);
+  for (int s = 0; s < 8; ++s) {
+    float b[2] = {0.f, 0.f};
+    if (I0 + 8 + s < I1) source_stats<VPT, DT>(src, I0 + 8 + s, wv, b[0], b[1]);
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int i = 2 * s + j;
-        const float give = upper ? v[i] : b[j];
-        const float keep = upper ? b[j] : v[i];
-        v[i] = keep + __shfl_xor_sync(FULL, give, 16);
-      }
+    for (int j = 0; j < 2; ++j) {
+      const int i = 2 * s + j;
+      const float give = upper ? v[i] : b[j];
+      const float keep = upper ? b[j] : v[i];
+      v[i] = keep + __shfl_xor_sync(FULL, give, 16);
     }
-    // the remaining steps of warp_transpose_reduce<32>
-#pragma unroll
-    for (int half = 8, o = 8; half >= 1; half >>= 1, o >>= 1) {
-      const bool up = (lane & o) != 0;
-#pragma unroll
-      for (int i = 0; i < half; ++i) {
-        const float give = up ? v[i] : v[i + half];
-        const float keep = up ? v[i + half] : v[i];
-        v[i] = keep + __shfl_xor_sync(FULL, give, o);
-      }
-    }
-    return v[0];
   }
+  // the remaining steps of warp_transpose_reduce<32>
+#pragma unroll
+  for (int half = 8, o = 8; half >= 1; half >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float give = up ? v[i] : v[i + half];
+      const float keep = up ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(FULL, give, o);
+    }
+  }
+  return v[0];
 }
 
 // Everything after the loads for one token: fold, sums, both exchanges,
@@ -797,7 +791,8 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
     src.fence();
     wt0 = warp_transpose_reduce<SL::KP0>(part0, lane);
   } else {
-    wt0 = sums_reduce<0, S0, SL::KP0, VPT, DT, true>(src, wv, lane);
+    static_assert(SL::KP0 == 32, "the second group exists only beside a full first one");
+    wt0 = sums_reduce_folded<0, S0, VPT, DT>(src, wv, lane);
     float part1[SL::KP1 > 0 ? SL::KP1 : 1];
     source_sums<16, S, (SL::KP1 > 0 ? SL::KP1 : 1), VPT, DT>(src, wv, part1);
     src.fence();
