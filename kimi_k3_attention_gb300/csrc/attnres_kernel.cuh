@@ -28,7 +28,8 @@
 //           evaluated by every warp redundantly (latency and deep shapes: all
 //           warps of all CTAs agree bitwise, no barrier), or by one warp and
 //           read by the others after a CTA barrier (the streaming shapes of
-//           up to 12 snapshots)
+//           up to 12 snapshots); the latency shapes keep the weights
+//           unnormalised, e_i = exp(l_i - max l), and apply their sum in r_h
 //   mix     h = sum_i alpha_i v_i from registers (no second read)
 //   R2      sum h^2: warp reduction, st.async to every CTA, mbarrier wait
 //   out     bf16(h * rsqrt(mean(h^2) + eps) * gamma) (FP16 for FP16 tensors)
@@ -466,6 +467,14 @@ __device__ __forceinline__ float half_warp_max(float v) {
   return v;
 }
 
+// The maximum over the warp in one instruction (sm_100 family); NaN lanes
+// are ignored, as by fmaxf.
+__device__ __forceinline__ float redux_max(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
@@ -861,6 +870,7 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
     return ex / den;
   };
   float alpha[S];
+  float den = 1.f;   // latency shapes: the sum of the unnormalised weights
   if constexpr (SMX) {
     // the streaming shapes of up to 12 snapshots: one warp evaluates the
     // softmax, the others read the weights after a CTA barrier (its next
@@ -877,6 +887,33 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < S; ++i) alpha[i] = x.alpha[i];
+  } else if constexpr (LAT) {
+    // Every warp evaluates it, with the shortest dependent chain in front of
+    // the mixture: lane i reads the pair (ss_i, d_i) of each CTA (the same
+    // additions, in the same order, as the totals above), the maximum is one
+    // redux.sync, and the mixture takes e_i = exp(l_i - max) while the sum
+    // of the e_i is formed beside it.  With h' = sum_i e_i v_i = den * h,
+    // RMSNorm(h) = h' * rsqrt(mean(h'^2) + eps * den^2) exactly, so den
+    // enters only r_h (and the tap's h = h' / den).  GB300, graphs of
+    // back-to-back calls, same-box A/B: -0.05 to -0.12 us on every decode
+    // shape (M <= 32, N = 1..12); out differs from the normalised form in
+    // a few elements by one BF16 ulp.
+    float ss_i = 0.f, d_i = 0.f;
+    if (lane < S) {
+#pragma unroll
+      for (uint32_t c = 0; c < 16; ++c)
+        if (c < t.csize) {
+          const float2 f = *reinterpret_cast<const float2*>(&x.xin1[c][2 * lane]);
+          ss_i += f.x;
+          d_i += f.y;
+        }
+    }
+    const float logit = (lane < S) ? rsqrtf(__fmaf_rn(ss_i, p.inv_h, p.eps)) * d_i : -INFINITY;
+    const float mx = redux_max(logit);
+    const float ex = (lane < S) ? __expf(logit - mx) : 0.f;
+    den = warp_sum(ex);   // lanes >= S add zeros: the same bits in every lane
+#pragma unroll
+    for (int i = 0; i < S; ++i) alpha[i] = __shfl_sync(FULL, ex, i);
   } else {
     // every warp evaluates it from identical totals in identical order:
     // bit-identical weights everywhere, no barrier
@@ -972,7 +1009,7 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
     for (int idx = lane; idx < nw_total; idx += 32) qq += x.xin2[idx];
     qq = warp_sum(qq);
   }
-  const float rh = rsqrtf(__fmaf_rn(qq, p.inv_h, p.eps));
+  const float rh = rsqrtf(__fmaf_rn(qq, p.inv_h, LAT ? p.eps * (den * den) : p.eps));
 
   // ---- outputs (after a timed-out exchange wait the sums are partial: out
   // and h_out are written as NaN, so that no wrong value passes as a
@@ -983,11 +1020,13 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
     if (ok[k]) {
       if (MODE != kNoFold && !LAT) st_out(p.new_prefix + row + jj[k], src.new_prefix(k));
       if (p.h_out != nullptr) {
+        // the latency shapes hold h' = den * h
+        const float hs = LAT ? 1.f / den : 1.f;
         uint4 hv;
-        hv.x = Fmt<DT>::pack(h[k][0], h[k][1]);
-        hv.y = Fmt<DT>::pack(h[k][2], h[k][3]);
-        hv.z = Fmt<DT>::pack(h[k][4], h[k][5]);
-        hv.w = Fmt<DT>::pack(h[k][6], h[k][7]);
+        hv.x = Fmt<DT>::pack(h[k][0] * hs, h[k][1] * hs);
+        hv.y = Fmt<DT>::pack(h[k][2] * hs, h[k][3] * hs);
+        hv.z = Fmt<DT>::pack(h[k][4] * hs, h[k][5] * hs);
+        hv.w = Fmt<DT>::pack(h[k][6] * hs, h[k][7] * hs);
         st_out(p.h_out + row + jj[k], t.failed ? nan4 : hv);
       }
       // (h * r_h) * gamma, two lanes per instruction, each product rounded
