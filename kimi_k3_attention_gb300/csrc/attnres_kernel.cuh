@@ -32,6 +32,8 @@
 //           unnormalised, e_i = exp(l_i - max l), and apply their sum in r_h
 //   mix     h = sum_i alpha_i v_i from registers (no second read)
 //   R2      sum h^2: warp reduction, st.async to every CTA, mbarrier wait
+//           (the latency shapes first add their warps' sums in the CTA and
+//           send one float per CTA)
 //   out     bf16(h * rsqrt(mean(h^2) + eps) * gamma) (FP16 for FP16 tensors)
 //           and new_prefix stored
 //
@@ -481,18 +483,6 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// The sum of L values (a power of two) in the order of an XOR butterfly over
-// L lanes (offsets L/2, ..., 1): the bits every lane of warp_sum (L = 32) or
-// half_warp_sum (L = 16) ends with when lane i starts with e[i].
-template <int L>
-__device__ __forceinline__ float butterfly_order_sum(float (&e)[L]) {
-#pragma unroll
-  for (int h = L / 2; h >= 1; h >>= 1)
-#pragma unroll
-    for (int i = 0; i < h; ++i) e[i] = e[i] + e[i + h];
-  return e[0];
-}
-
 // Transpose-reduction of KP (a power of two <= 32) values per lane across the
 // warp with KP-1 + (5 - log2 KP) shuffles.  Afterwards lane l holds the warp
 // total of value index l >> (5 - log2 KP); lanes sharing an index agree.
@@ -549,13 +539,17 @@ struct Sums {
 //   red:  per-warp partials of R1 (local)
 //   xin1: R1 totals pushed by each CTA of the cluster (st.async), by rank
 //   xin2: per-warp sums of h^2 pushed by each CTA, index rank * warps + warp
+//         (latency shapes: one CTA sum each, index rank)
+//   red2: per-warp sums of h^2 (local; latency shapes)
 //   bar1, bar2: mbarriers counting the bytes of xin1 / xin2 of one token
 // Protocol per token k (phase parity k & 1 on both mbarriers):
 //   R1: warp 0 of every CTA stores its Sums<N>::total totals into
 //       xin1[rank] of every CTA with st.async; every thread waits on bar1; thread 0 then re-arms
 //       bar1 for token k+1.
-//   R2: lane c of every warp stores the warp's sum of h^2 into CTA c; every
-//       thread waits on bar2; thread 0 re-arms bar2.
+//   R2: lane c of every warp stores the warp's sum of h^2 into CTA c (the
+//       latency shapes: lane c of warp 0 stores the CTA's sum, formed from
+//       red2 after a CTA barrier); every thread waits on bar2; thread 0
+//       re-arms bar2.
 // A peer's next store into xin1 (token k+1) needs this CTA's R2(k) stores,
 // which follow this CTA's reads of xin1(k) and its re-arm of bar1; its next
 // store into xin2 needs this CTA's R1(k+1) stores, which follow the reads of
@@ -569,6 +563,7 @@ struct alignas(16) Exchange {
   float xin1[16][32 * G];  // up to 16 CTAs per cluster
   float xin2[256];         // 16 CTAs x 16 warps
   float alpha[32 * G];     // softmax weights (shapes where one warp evaluates it)
+  float red2[16];          // per-warp sums of h^2 (latency shapes)
   unsigned long long bar1;
   unsigned long long bar2;
 };
@@ -581,25 +576,27 @@ struct Thread {
 };
 
 // Bytes each CTA expects per token: kp (Sums<N>::total) totals from every
-// CTA (R1) and one float per warp of every CTA (R2).
+// CTA (R1) and one float per warp of every CTA (R2), or one per CTA where
+// the CTA sums its warps first (CTA_R2: the latency shapes).
 __device__ __forceinline__ uint32_t r1_bytes(int kp, const Thread& t, const Params& p) {
   return static_cast<uint32_t>(kp) * t.csize * 4u + p.extra_tx;
 }
+template <bool CTA_R2>
 __device__ __forceinline__ uint32_t r2_bytes(const Thread& t, const Params& p) {
-  return static_cast<uint32_t>(t.nwarps) * t.csize * 4u + p.extra_tx;
+  return (CTA_R2 ? 1u : static_cast<uint32_t>(t.nwarps)) * t.csize * 4u + p.extra_tx;
 }
 
 // Once per kernel, before the first exchange: thread 0 initialises and arms
 // both mbarriers; the start of the cluster handshake (arrive now, wait
 // before the first remote store) both publishes them and guarantees every
 // CTA of the cluster runs.
-template <int KP, int G>
+template <int KP, bool CTA_R2, int G>
 __device__ __forceinline__ void exchange_init(Exchange<G>& x, const Thread& t, const Params& p) {
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&x.bar1), 1);
     mbar_init(smem_u32(&x.bar2), 1);
     mbar_arm(smem_u32(&x.bar1), r1_bytes(KP, t, p));
-    mbar_arm(smem_u32(&x.bar2), r2_bytes(t, p));
+    mbar_arm(smem_u32(&x.bar2), r2_bytes<CTA_R2>(t, p));
     fence_mbar_init();
   }
   cluster_arrive_relaxed();
@@ -978,34 +975,38 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
   }
 
   // ---- R2: warp sum, lane c stores it into CTA c, every warp sums all
-  // warps of all CTAs in one fixed order
+  // warps of all CTAs in one fixed order.  The latency shapes add the warps'
+  // sums in the CTA first (a CTA barrier) and send one float per CTA: GB300,
+  // same-box A/B, -0.02 to -0.08 us on every decode shape against 4-8 floats
+  // per CTA and 16-32 partials summed in every lane
   q = warp_sum(q);
-  if (static_cast<uint32_t>(lane) < t.csize)
-    st_async_f32(dsmem_map(smem_u32(&x.xin2[t.crank * t.nwarps + warp]), lane), q,
-                 dsmem_map(bar2, lane));
+  if constexpr (LAT) {
+    if (lane == 0) x.red2[warp] = q;
+    __syncthreads();
+    if (warp == 0) {
+      float sq = 0.f;
+#pragma unroll
+      for (int w = 0; w < 16; ++w)
+        if (w < t.nwarps) sq += x.red2[w];
+      if (static_cast<uint32_t>(lane) < t.csize)
+        st_async_f32(dsmem_map(smem_u32(&x.xin2[t.crank]), lane), sq, dsmem_map(bar2, lane));
+    }
+  } else {
+    if (static_cast<uint32_t>(lane) < t.csize)
+      st_async_f32(dsmem_map(smem_u32(&x.xin2[t.crank * t.nwarps + warp]), lane), q,
+                   dsmem_map(bar2, lane));
+  }
   exchange_wait(bar2, t, p);
-  if (threadIdx.x == 0 && !t.failed) mbar_arm(bar2, r2_bytes(t, p));  // next token
+  if (threadIdx.x == 0 && !t.failed) mbar_arm(bar2, r2_bytes<LAT>(t, p));  // next token
   t.phase ^= 1u;
-  const int nw_total = static_cast<int>(t.csize) * t.nwarps;
   float qq = 0.f;
   if constexpr (LAT) {
-    // every lane adds all partials itself: v[l] as lane l would (xin2[l],
-    // xin2[l + 32], ... in order), then the butterfly's pairing of lanes
-    float v[32];
+    // every lane adds the CTAs' sums in rank order
 #pragma unroll
-    for (int l = 0; l < 32; ++l) v[l] = 0.f;
-    for (int base = 0; base < nw_total; base += 32) {
-#pragma unroll
-      for (int l4 = 0; l4 < 8; ++l4) {
-        const float4 f = *reinterpret_cast<const float4*>(&x.xin2[base + 4 * l4]);
-        if (base + 4 * l4 < nw_total) v[4 * l4] += f.x;
-        if (base + 4 * l4 + 1 < nw_total) v[4 * l4 + 1] += f.y;
-        if (base + 4 * l4 + 2 < nw_total) v[4 * l4 + 2] += f.z;
-        if (base + 4 * l4 + 3 < nw_total) v[4 * l4 + 3] += f.w;
-      }
-    }
-    qq = butterfly_order_sum<32>(v);
+    for (uint32_t c = 0; c < 16; ++c)
+      if (c < t.csize) qq += x.xin2[c];
   } else {
+    const int nw_total = static_cast<int>(t.csize) * t.nwarps;
     for (int idx = lane; idx < nw_total; idx += 32) qq += x.xin2[idx];
     qq = warp_sum(qq);
   }
@@ -1118,7 +1119,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
   // streaming regime after the first token's loads are issued, so that the
   // set-up does not delay them.
   const bool early_init = p.prefetch != 0;
-  if (early_init && m0 < p.M) exchange_init<Sums<N>::total>(x, t, p);
+  if (early_init && m0 < p.M) exchange_init<Sums<N>::total, LAT>(x, t, p);
   // Latency regime, bit 3: before the wait, read one 32-bit word of every
   // 128-byte line of this CTA's first-token rows (through L2 only, never
   // allocated in L1).  On GB300 lines an SM has read are served to it faster
@@ -1195,7 +1196,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_fused_kernel(const Params 
     // Let the next kernel on the stream be scheduled once every CTA of this
     // grid is past its first loads; it still waits for this grid to finish.
     if (m == m0) griddep_launch_dependents();
-    if (!early_init && m == m0) exchange_init<Sums<N>::total>(x, t, p);
+    if (!early_init && m == m0) exchange_init<Sums<N>::total, LAT>(x, t, p);
     if constexpr (HYB) {
       cp_async_wait<0>();   // this thread's own slots: no barrier needed
       HybridSources<N, NR> src{v, hyb0, hstep, ok[0]};
@@ -1231,7 +1232,7 @@ __global__ void __launch_bounds__(MAXT, MINB) attnres_pipe_kernel(const Params p
   const uint32_t row_step = blockDim.x * 16u;
   const uint32_t stage_step = ROWS * row_step;
 
-  exchange_init<Sums<N>::total>(x, t, p);
+  exchange_init<Sums<N>::total, false>(x, t, p);
   griddep_wait();
   const uint4 wv[1] = {ok[0] ? ld_keep(p.w + jj1) : make_uint4(0, 0, 0, 0)};
   const uint4 gv[1] = {ok[0] ? ld_keep(p.gamma + jj1) : make_uint4(0, 0, 0, 0)};
