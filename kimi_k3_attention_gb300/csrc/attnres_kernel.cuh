@@ -22,8 +22,9 @@
 //   R1      2(N+1) partial sums: warp transpose-reduction (one per group of
 //           up to 16 sources, see Sums), CTA sum in shared
 //           memory, then every CTA stores its totals into the shared memory
-//           of every CTA of the cluster with st.async, each store counted on
-//           the receiver's mbarrier, which the receiver waits on
+//           of every CTA of the cluster with st.async (one warp per receiving
+//           CTA in the latency shapes), each store counted on the receiver's
+//           mbarrier, which the receiver waits on
 //   softmax logits and softmax from the cluster totals in a fixed order:
 //           evaluated by every warp redundantly (latency and deep shapes: all
 //           warps of all CTAs agree bitwise, no barrier), or by one warp and
@@ -539,17 +540,21 @@ struct Sums {
 //   red:  per-warp partials of R1 (local)
 //   xin1: R1 totals pushed by each CTA of the cluster (st.async), by rank
 //   xin2: per-warp sums of h^2 pushed by each CTA, index rank * warps + warp
-//         (latency shapes: one CTA sum each, index rank)
-//   red2: per-warp sums of h^2 (local; latency shapes)
+//         (latency shapes: one CTA sum each, index rank; their per-warp sums
+//         of h^2 are kept locally in xin2[128..143], which no CTA stores to)
 //   bar1, bar2: mbarriers counting the bytes of xin1 / xin2 of one token
 // Protocol per token k (phase parity k & 1 on both mbarriers):
 //   R1: warp 0 of every CTA stores its Sums<N>::total totals into
-//       xin1[rank] of every CTA with st.async; every thread waits on bar1; thread 0 then re-arms
-//       bar1 for token k+1.
+//       xin1[rank] of every CTA with st.async (the latency shapes: warp c
+//       into CTA c); every thread waits on bar1; thread 0 then re-arms
+//       bar1 for token k+1.  The next write into red follows, in every warp,
+//       the token's R2: after R2's CTA barrier in the latency shapes (which
+//       every sending warp reaches after its sends), else after the R1 wait,
+//       which needs warp 0's own store, made after its reads of red.
 //   R2: lane c of every warp stores the warp's sum of h^2 into CTA c (the
 //       latency shapes: lane c of warp 0 stores the CTA's sum, formed from
-//       red2 after a CTA barrier); every thread waits on bar2; thread 0
-//       re-arms bar2.
+//       the warps' sums after a CTA barrier); every thread waits on bar2;
+//       thread 0 re-arms bar2.
 // A peer's next store into xin1 (token k+1) needs this CTA's R2(k) stores,
 // which follow this CTA's reads of xin1(k) and its re-arm of bar1; its next
 // store into xin2 needs this CTA's R1(k+1) stores, which follow the reads of
@@ -563,7 +568,6 @@ struct alignas(16) Exchange {
   float xin1[16][32 * G];  // up to 16 CTAs per cluster
   float xin2[256];         // 16 CTAs x 16 warps
   float alpha[32 * G];     // softmax weights (shapes where one warp evaluates it)
-  float red2[16];          // per-warp sums of h^2 (latency shapes)
   unsigned long long bar1;
   unsigned long long bar2;
 };
@@ -815,7 +819,11 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
     cluster_wait();
     first = false;
   }
-  if (warp == 0) {
+  // Warp 0 forms the CTA's totals and stores them into every CTA; in the
+  // latency shapes warps 0..C-1 each form them (the same additions in the
+  // same order) and warp c stores into CTA c (GB300, same-box A/B: -0.01 to
+  // -0.06 us on 15 of 16 decode shapes, M = 32, N = 12 unchanged).
+  if (LAT ? static_cast<uint32_t>(warp) < t.csize : warp == 0) {
 #pragma unroll
     for (int g = 0; g < SL::G; ++g) {
       const int kp = g == 0 ? SL::KP0 : SL::KP1;
@@ -825,7 +833,12 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
         for (int w = 0; w < 16; ++w)
           if (w < t.nwarps) s += x.red[w][32 * g + lane];
         const uint32_t a = smem_u32(&x.xin1[t.crank][32 * g + lane]);
-        for (uint32_t c = 0; c < t.csize; ++c) st_async_f32(dsmem_map(a, c), s, dsmem_map(bar1, c));
+        if (LAT) {
+          for (uint32_t c = warp; c < t.csize; c += t.nwarps)
+            st_async_f32(dsmem_map(a, c), s, dsmem_map(bar1, c));
+        } else {
+          for (uint32_t c = 0; c < t.csize; ++c) st_async_f32(dsmem_map(a, c), s, dsmem_map(bar1, c));
+        }
       }
     }
   }
@@ -981,13 +994,17 @@ __device__ __forceinline__ void token_epilogue(const Params& p, Exchange<Sums<N>
   // per CTA and 16-32 partials summed in every lane
   q = warp_sum(q);
   if constexpr (LAT) {
-    if (lane == 0) x.red2[warp] = q;
+    // the warps' sums in xin2[128..] rather than in a member of their own:
+    // 64 more bytes of static shared memory cost the N = 12 streaming
+    // shapes 1-2 % (GB300, same-box A/B)
+    float* red2 = &x.xin2[128];
+    if (lane == 0) red2[warp] = q;
     __syncthreads();
     if (warp == 0) {
       float sq = 0.f;
 #pragma unroll
       for (int w = 0; w < 16; ++w)
-        if (w < t.nwarps) sq += x.red2[w];
+        if (w < t.nwarps) sq += red2[w];
       if (static_cast<uint32_t>(lane) < t.csize)
         st_async_f32(dsmem_map(smem_u32(&x.xin2[t.crank]), lane), sq, dsmem_map(bar2, lane));
     }
