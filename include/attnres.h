@@ -133,15 +133,17 @@ int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
  *                 CTA owning a contiguous 1/cluster of the columns, 8 columns
  *                 per thread (<= 256 threads); the per-token sums are
  *                 exchanged through distributed shared memory;
- *             3 = as 2 with at most 224 threads and registers capped so that
- *                 three CTAs share an SM (four while a token has at most 12
- *                 rows: N <= 9 with add2, N <= 10 without, N <= 11
- *                 without the fold);
+ *             3 = as 2 with at most 224 threads and registers capped by the
+ *                 rows a token has (bank, prefix and addends): at 56 (five
+ *                 CTAs of 224 threads share an SM) up to 6 rows, else at 72
+ *                 (four), with the bank rows past the first 11-12 rows in
+ *                 the thread's own slots of shared memory;
  *             5 = as 2 with registers capped so that two CTAs of up to 256
  *                 threads share an SM (in back-to-back calls the next
  *                 call's CTAs can become resident, and prefetch, while this
  *                 call runs); the automatic choice from 17 to 32 tokens
- *                 when the call folds BF16 tensors and N <= 12;
+ *                 when the call folds BF16 tensors and N <= 12, with 4 to
+ *                 8 CTAs per token chosen per M (measured on GB300);
  *             Variants 1, 4 and 5 exist for N <= 12 only (variant 5 with
  *             the fold on BF16 tensors only).  For N > 12
  *             variant 3 takes at most 128 threads, registers capped so

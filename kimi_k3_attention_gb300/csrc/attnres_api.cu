@@ -162,6 +162,20 @@ constexpr size_t kPipeSmemMax = 227 * 1024 - sizeof(Exchange<1>) - 1024;
 // check the result.  bf16_fold: the call folds BF16 tensors (the shapes
 // compiled for that case only may be chosen).  Returns ATTNRES_OK or
 // ATTNRES_ERR_CONFIG.
+// Cluster size per token of the register-capped split shape (variant 5) at
+// H = 7168 for M = 17..28, the fastest of 4..8 CTAs in same-box sweeps on
+// GB300 (graphs of back-to-back calls, warm and cold), taken for tokens of
+// at least 9 rows (bank, prefix, addends); tokens with fewer rows, and 29 to
+// 32 tokens, keep about 128 / M CTAs (4 from 29 tokens on: 7-8 CTAs were
+// within 0.05 us of it there, faster or slower depending on the run).  The
+// sizes that fill 120-140 SMs win below 26 tokens; from there on the calls
+// whose CTAs come close to every SM (6 CTAs from 24 tokens, 5 from 29) lose
+// 0.3-0.8 us, presumably to clusters placed on SMs that already hold one of
+// the same call, and 8 CTAs (two per SM on most SMs) are fastest.  N = 12:
+// M = 26-28 2.95-2.97 us against 3.09-3.14 for 5 CTAs; M = 17-18 2.69-2.71
+// against 2.81-2.82 for 7-8.
+constexpr int kSplit2Cluster[12] = {4, 4, 6, 6, 6, 6, 6, 5, 5, 8, 8, 8};
+
 int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c, bool bf16_fold) {
   const int H8 = H / 8;
   auto min_cluster = [&](int maxt) {
@@ -178,12 +192,13 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c, bool bf1
     // Measured on GB300 at H = 7168 (the cluster sizes below are for that
     // H and scale with it): up to 32 tokens, a cluster of about 128 / M CTAs
     // (clamped to 4..8) per token keeps ~128 CTAs per call, one per SM; from
-    // 17 tokens on (4 CTAs of 224 threads) with registers capped so that
+    // 17 tokens on, with the fold on BF16 tensors, registers capped so that
     // the next call's CTAs fit beside them (0.05-0.16 us faster there, the
-    // same below); up to 48 tokens, 8 CTAs of 112 columns (three fit an SM,
-    // still one wave); then the register-capped shape, 4 CTAs of 224
-    // columns up to 96 tokens and 7 CTAs of 128 columns beyond, where many
-    // tokens are in flight on every SM.  Deep banks: up to 32 tokens the
+    // same below), and the cluster size from kSplit2Cluster; up to 48
+    // tokens, 8 CTAs of 112 columns (three fit an SM, still one wave); then
+    // the register-capped shape, 4 CTAs of 224 columns up to 96 tokens and
+    // 7 CTAs of 128 columns beyond, where many tokens are in flight on every
+    // SM.  Deep banks: up to 32 tokens the
     // same clusters (4 CTAs from 8 tokens on once N >= 24, where a token's
     // rows are many), beyond that their streaming shape, 7 CTAs of 128
     // columns (the split shape's CTAs hold too many registers to share an
@@ -193,6 +208,7 @@ int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c, bool bf1
       c->variant = (M >= 17 && bf16_fold && !deep) ? 5 : 2;
       ref = (128 + M / 2) / M;
       ref = ref < 4 ? 4 : (ref > 8 ? 8 : ref);
+      if (c->variant == 5 && M <= 28 && N + (add2 ? 3 : 2) >= 9) ref = kSplit2Cluster[M - 17];
       if (N >= 24 && M >= 8) ref = 4;
     } else if (deep) {
       c->variant = 3;

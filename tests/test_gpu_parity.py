@@ -46,6 +46,28 @@ def test_decode_sweep_auto(case):
     assert_parity(inp, gnp, gout, label=f"case {idx}")
 
 
+# the automatic cluster size of the register-capped split shape, per M, for
+# tokens of at least 9 rows up to M = 28; otherwise about 128 / M (4 from 29)
+SPLIT2_CLUSTER = {17: 4, 18: 4, 19: 6, 20: 6, 21: 6, 22: 6, 23: 6, 24: 5, 25: 5, 26: 8, 27: 8,
+                  28: 8, 29: 4, 30: 4, 31: 4, 32: 4}
+
+
+@pytest.mark.parametrize("M", sorted(SPLIT2_CLUSTER))
+def test_decode_auto_every_M_17_to_32(M):
+    """Every token count of the register-capped split shape with its
+    automatic cluster size (4 to 8 CTAs of 224 to 112 threads), with and
+    without add2: parity with the oracle."""
+    for N, add2 in ((12, True), (9, False), (3, False)):
+        rows = N + (3 if add2 else 2)
+        want = (SPLIT2_CLUSTER[M] if rows >= 9
+                else min(8, max(4, (128 + M // 2) // M)))
+        plan = binding.attnres_plan(M, N, H, has_add2=add2)
+        assert plan["variant"] == 5 and plan["cluster"] == want, (N, add2, plan)
+        inp = wl.make_inputs(M, N, H, seed=300 + M + N, add2=add2)
+        gnp, gout = run_gpu(inp)
+        assert_parity(inp, gnp, gout, label=f"M={M} N={N}")
+
+
 @pytest.mark.parametrize("cfg", split_configs(H)[1:], ids=cfg_name)
 @pytest.mark.parametrize("M,N", [(1, 12), (32, 12), (16, 5), (8, 1)])
 def test_decode_every_variant(cfg, M, N):
