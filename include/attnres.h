@@ -327,6 +327,12 @@ int attnres_launch(const attnres_args* args, const attnres_config* cfg,
  * reads the SM count). */
 int attnres_plan(int M, int N, int H, int has_add2, attnres_config* plan);
 
+/* The same choice computed on the host alone, without a CUDA device (the
+ * choice depends on M, N, H and the second addend only; a launch still
+ * checks that the current device is a compute capability 10.3 GPU).
+ * Returns a status. */
+int attnres_plan_host(int M, int N, int H, int has_add2, attnres_config* plan);
+
 /* Static description of a status code; never NULL. */
 const char* attnres_status_string(int status);
 

@@ -35,6 +35,7 @@ EXPORTS = (
     "attnres_access_pattern",
     "attnres_launch",
     "attnres_plan",
+    "attnres_plan_host",
     "attnres_status_string",
     "attnres_last_cuda_error",
     "attnres_device_status",
@@ -89,6 +90,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.attnres_add_rmsnorm_ex.restype = i
     lib.attnres_plan.argtypes = [i, i, i, i, ctypes.POINTER(Config)]
     lib.attnres_plan.restype = i
+    lib.attnres_plan_host.argtypes = [i, i, i, i, ctypes.POINTER(Config)]
+    lib.attnres_plan_host.restype = i
     lib.attnres_status_string.argtypes = [i]
     lib.attnres_status_string.restype = ctypes.c_char_p
     lib.attnres_last_cuda_error.argtypes = []
@@ -303,6 +306,13 @@ def attnres_add_rmsnorm_raw(prefix, add, add2, bank, w, gamma, eps, out, new_pre
 def attnres_plan(M, N, H, has_add2=True) -> dict:
     c = Config()
     _check(load().attnres_plan(int(M), int(N), int(H), int(bool(has_add2)), ctypes.byref(c)))
+    return c.as_dict()
+
+
+def attnres_plan_host(M, N, H, has_add2=True) -> dict:
+    """The automatic launch configuration, computed without a CUDA device."""
+    c = Config()
+    _check(load().attnres_plan_host(int(M), int(N), int(H), int(bool(has_add2)), ctypes.byref(c)))
     return c.as_dict()
 
 

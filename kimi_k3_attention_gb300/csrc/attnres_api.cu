@@ -176,7 +176,7 @@ constexpr size_t kPipeSmemMax = 227 * 1024 - sizeof(Exchange<1>) - 1024;
 // against 2.81-2.82 for 7-8.
 constexpr int kSplit2Cluster[12] = {4, 4, 6, 6, 6, 6, 6, 5, 5, 8, 8, 8};
 
-int resolve(int M, int N, bool add2, int H, int sms, attnres_config* c, bool bf16_fold) {
+int resolve(int M, int N, bool add2, int H, attnres_config* c, bool bf16_fold) {
   const int H8 = H / 8;
   auto min_cluster = [&](int maxt) {
     int cl = 1;
@@ -444,7 +444,7 @@ int run(const Args& a, const attnres_config* cfg, cudaStream_t s) {
   if ((st = current_device(&sms)) != ATTNRES_OK) return st;
   const bool has_add2 = a.fold && a.add2 != nullptr;
   attnres_config c = cfg ? *cfg : attnres_config{0, 0, 0, 0, 0, 0, 0, 0};
-  if ((st = resolve(a.M, a.N, has_add2, a.H, sms, &c, a.fold && a.dtype == ATTNRES_DTYPE_BF16)) !=
+  if ((st = resolve(a.M, a.N, has_add2, a.H, &c, a.fold && a.dtype == ATTNRES_DTYPE_BF16)) !=
       ATTNRES_OK)
     return st;
   // the attention-residual alone and FP16 tensors exist in the two fused
@@ -674,7 +674,7 @@ extern "C" int attnres_access_pattern(const void* prefix, const void* add, const
   int sms = 0;
   if ((st = current_device(&sms)) != ATTNRES_OK) return st;
   attnres_config c = {0, 0, 0, 0, 0, 0, 0, 0};
-  if ((st = resolve(M, N, true, H, sms, &c, true)) != ATTNRES_OK) return st;
+  if ((st = resolve(M, N, true, H, &c, true)) != ATTNRES_OK) return st;
   if (c.threads > kPatternMaxT) return ATTNRES_ERR_CONFIG;
   Params p = {};
   p.prefix = static_cast<const uint4*>(prefix);
@@ -702,7 +702,17 @@ extern "C" int attnres_plan(int M, int N, int H, int has_add2, attnres_config* p
   int st = current_device(&sms);
   if (st != ATTNRES_OK) return st;
   attnres_config c = {0, 0, 0, 0, 0, 0, 0, 0};
-  if ((st = resolve(M, N, has_add2 != 0, H, sms, &c, true)) != ATTNRES_OK) return st;
+  if ((st = resolve(M, N, has_add2 != 0, H, &c, true)) != ATTNRES_OK) return st;
+  *plan = c;
+  return ATTNRES_OK;
+}
+
+extern "C" int attnres_plan_host(int M, int N, int H, int has_add2, attnres_config* plan) {
+  if (!plan) return ATTNRES_ERR_NULL;
+  if (validate_shape(M, N, H) != ATTNRES_OK) return ATTNRES_ERR_SHAPE;
+  attnres_config c = {0, 0, 0, 0, 0, 0, 0, 0};
+  const int st = resolve(M, N, has_add2 != 0, H, &c, true);
+  if (st != ATTNRES_OK) return st;
   *plan = c;
   return ATTNRES_OK;
 }
