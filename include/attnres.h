@@ -118,7 +118,8 @@ typedef enum {
  * PR's other fallback) is fused here too, in variant 2 only; N > 31 is
  * rejected with ATTNRES_ERR_SHAPE (the sums of 32 sources fill two warp-wide
  * reductions).
- * The launch configuration is chosen from (M, N, H) and the SM count.
+ * The launch configuration is chosen from M, N, H and the presence of add2
+ * (attnres_plan reports it).
  */
 int attnres_add_rmsnorm(const void* prefix, const void* add, const void* add2,
                         const void* bank, const void* w, const void* gamma,
